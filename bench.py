@@ -1,0 +1,391 @@
+"""Benchmark of the paged GQA attention hot path on GB300.
+
+One step = RoPE-and-append of the batch's new tokens into the block arena,
+then paged attention of those tokens over the arena (the whole hot path of
+pages "Building Kshipra" part 3, sections 1 and 4), on the Llama-3-8B-shaped
+decode batch (64 sequences, contexts 512-4096, 32 q / 8 kv heads, head dim
+128, fp16, block size 16) unless --workload says otherwise.
+
+metric: decode KV-read GB/s = algorithmic KV bytes (keys and values of every
+context token, each read once) / step time.  A secondary object measures the
+chunked-prefill workload in TFLOP/s (4 x head_dim x q heads x visible
+(query, key) pairs per call).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {kshipra,reference}]
+Multi-GPU runs (torchrun) run one independent replica per GPU.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    try:
+        with open(MEASURED_PEAKS) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ work sizes
+
+def decode_kv_bytes(w, seqs=None) -> int:
+    """Keys and values of every context token of the chosen sequences."""
+    ctx = w.context_lens.astype(np.int64)
+    if seqs is not None:
+        ctx = ctx[seqs]
+    return int(ctx.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+
+
+def visible_pairs(w) -> int:
+    """Causal (query, key) pairs: a query at position p sees keys 0..p."""
+    return int((w.positions.astype(np.int64) + 1).sum())
+
+
+def attention_flops(w) -> float:
+    return 4.0 * w.head_dim * w.num_q_heads * visible_pairs(w)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while running (SM clock, reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.text = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.text, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.text, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = list(csv.reader(io.StringIO(self.text)))
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def _events(torch, n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def time_steps(torch, dw, steps, warmup, stream, flush=None):
+    """Times `steps` whole steps (append + attention) on `stream`.
+
+    Returns (total_ms, per-step append ms list, per-step attention ms list).
+    Events bracket each call on the launching stream.  When `flush` is given
+    (a byte buffer larger than L2), it is overwritten between steps, outside
+    the timed windows.
+    """
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            dw.step(stream=stream)
+    torch.cuda.synchronize()
+    ev = _events(torch, 3 * steps)
+    t0, t1 = _events(torch, 2)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(steps):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+            ev[3 * i].record(stream)
+            dw.append_step(stream=stream)
+            ev[3 * i + 1].record(stream)
+            dw.attention(stream=stream)
+            ev[3 * i + 2].record(stream)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    app = [ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(steps)]
+    att = [ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(steps)]
+    if flush is None:
+        total = t0.elapsed_time(t1)
+    else:  # the flushes are not part of the work
+        total = sum(ev[3 * i].elapsed_time(ev[3 * i + 2]) for i in range(steps))
+    return total, app, att
+
+
+def time_e2e(torch, dw, steps, stream):
+    """Same step through the public API from pinned host buffers: H2D of the
+    step's inputs, append + attention, D2H of the output, every step."""
+    w = dw.w
+    host = {}
+    for name in ("q", "k_new", "v_new", "block_tables", "context_lens", "query_start_loc", "positions"):
+        t = getattr(dw, name)
+        host[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+    out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    t0, t1 = _events(torch, 2)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(steps):
+            for name, h in host.items():
+                getattr(dw, name).copy_(h, non_blocking=True)
+            dw.step(stream=stream)
+            out_host.copy_(dw.out, non_blocking=True)
+            stream.synchronize()  # the caller reads the result every step
+        t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), h2d, d2h
+
+
+def gpu_launches_per_step(w, decode_max_rows=16):
+    G = w.num_q_heads // w.num_kv_heads
+    rows = w.query_lens * G
+    n = 1 + 1  # append, decode
+    import paged_kv_cache_arena_gb300 as K
+    ws = K.kshipra_paged_attention_workspace_size(w.num_seqs, w.num_tokens, w.max_context_len, w.num_q_heads,
+                                                  w.num_kv_heads, w.head_dim)
+    if ws > 0:
+        n += 1  # combine
+    if (rows > decode_max_rows).any():
+        n += 1  # prefill
+    return n
+
+
+def measure_prefill(torch, stream, pk):
+    """Secondary object: chunked-prefill attention TFLOP/s (L2 flushed)."""
+    from workloads import make_config
+    from workloads.device import DeviceWorkload
+    w = make_config("chunked-prefill")
+    dw = DeviceWorkload(w)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    steps = 50
+    total, app, att = time_steps(torch, dw, steps, 5, stream, flush=flush)
+    att_ms = statistics.mean(att)
+    flops = attention_flops(w)
+    tflops = flops / (att_ms * 1e-3) / 1e12
+    peak = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    return {"workload": "chunked-prefill", "metric": "chunked-prefill attention TFLOP/s", "unit": "TFLOP/s",
+            "value": round(tflops, 2), "ms_per_call": round(att_ms, 5), "flops_per_call": flops,
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(tflops / peak, 4), "traffic": None,
+                         "peak_note": "fp16 dense = bf16 dense rate (measured cuBLAS bf16 burst)"},
+            "l2": "flushed between calls (512 MiB write)"}
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+
+def oracle_sample(w, budget_s: float = 15.0):
+    """Times the float64 oracle on whole sequences of the workload, adding
+    sequences until about `budget_s` seconds of CPU work.  Returns
+    (seconds, kv_bytes, flops, n_seqs, threads)."""
+    import oracle
+    threads = oracle.default_threads()
+    qsl = w.query_start_loc
+    order = list(range(w.num_seqs))
+    done, secs = [], 0.0
+    per = None
+    while order and secs < budget_s:
+        take = 1 if per is None else max(1, min(len(order), int((budget_s - secs) / max(per, 1e-6))))
+        batch, order = order[:take], order[take:]
+        toks = np.concatenate([np.arange(qsl[s], qsl[s + 1]) for s in batch]).astype(np.int32)
+        t = time.perf_counter()
+        oracle.workload_attention(w, tokens=toks, nthreads=threads)
+        dt = time.perf_counter() - t
+        secs += dt
+        done += batch
+        per = secs / len(done)
+    kv = decode_kv_bytes(w, np.array(done))
+    pairs = int(sum((w.positions[qsl[s]:qsl[s + 1]].astype(np.int64) + 1).sum() for s in done))
+    flops = 4.0 * w.head_dim * w.num_q_heads * pairs
+    return secs, kv, flops, len(done), threads
+
+
+def reference_arm(args, w):
+    """The oracle as the reference implementation: each step is a bounded
+    sample of the same workload, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, budget_s=budget / 4)
+    secs = kv = 0.0
+    n_seqs = threads = 0
+    for _ in range(args.steps):
+        s_, kv_, _, n_, threads = oracle_sample(w, budget_s=budget)
+        secs += s_
+        kv += kv_
+        n_seqs = n_
+    value = kv / secs / 1e9
+    line = {"impl": "reference", "metric": "decode KV-read GB/s", "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "num_seqs": w.num_seqs, "context": "512-4096",
+                       "heads": "%dq/%dkv" % (w.num_q_heads, w.num_kv_heads), "head_dim": w.head_dim,
+                       "block_size": w.block_size, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": "first %d of %d sequences per step (all q heads), float64 C oracle"
+                                       % (n_seqs, w.num_seqs)},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main
+
+def gpu_arm(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_arena_gb300 as K
+    from workloads.device import DeviceWorkload
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    K._lib.load()  # fails loudly when the library is not built
+    pk, pk_src = peaks()
+    dw = DeviceWorkload(w)
+    stream = torch.cuda.Stream()
+    kv = decode_kv_bytes(w)
+    try:
+        smi_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        smi_id = str(local)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(smi_id) as clk:
+        barrier()
+        total_ms, app, att = time_steps(torch, dw, args.steps, args.warmup, stream)
+        barrier()
+    clocks = clk.summary()
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = K.kshipra_device_status()
+    ms_step = total_ms / args.steps
+    value = world * kv * args.steps / (total_ms * 1e-3) / 1e9
+    att_ms = statistics.mean(att)
+    achieved = kv / (att_ms * 1e-3) / 1e9
+    e2e_steps = min(args.steps, 300)
+    e2e_ms, h2d, d2h = time_e2e(torch, dw, e2e_steps, stream)
+    e2e_value = world * kv * e2e_steps / (e2e_ms * 1e-3) / 1e9
+    secondary = None
+    if not args.no_prefill:
+        try:
+            secondary = measure_prefill(torch, stream, pk)
+        except Exception as exc:  # reported, never silently substituted
+            secondary = {"workload": "chunked-prefill", "error": str(exc)[:200]}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, kv_s, _, n_s, threads = oracle_sample(w)
+        cpu = {"value": round(kv_s / secs / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": "%d of %d sequences, all q heads, float64 C oracle, %.1f s" % (n_s, w.num_seqs, secs)}
+    launches = gpu_launches_per_step(w) * args.steps
+    if rank == 0:
+        line = {
+            "metric": "decode KV-read GB/s", "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16" if w.dtype == "f16" else "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "num_seqs": w.num_seqs, "context_lens": "%d-%d" % (
+                int(w.context_lens.min()), int(w.context_lens.max())),
+                "heads": "%dq/%dkv" % (w.num_q_heads, w.num_kv_heads), "head_dim": w.head_dim,
+                "block_size": w.block_size, "kv_bytes_per_step": kv, "parallelism": "replicas" if world > 1 else "single",
+                "l2": "inputs larger than L2 (%.0f MB of KV per step)" % (kv / 1e6)},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk.get("hbm_gbs"),
+                         "unit": "GB/s", "frac": round(achieved / pk.get("hbm_gbs"), 4), "traffic": None,
+                         "kernel": "paged attention call (decode_kernel + combine_kernel)",
+                         "ms_per_launch": round(att_ms, 5), "peak_source": pk_src},
+            "append_ms_per_step": round(statistics.mean(app), 5),
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": launches, "clocks": clocks, "device_status": status,
+            "cpu_baseline": cpu, "secondary": secondary,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["kshipra", "reference"], default="kshipra")
+    ap.add_argument("--workload", default="llama-decode", choices=["llama-decode", "long-decode", "mixed"])
+    ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill secondary object")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from workloads import make_config
+    w = make_config(args.workload)
+    if args.impl == "reference":
+        reference_arm(args, w)
+    else:
+        gpu_arm(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * kshipra.h -- C ABI of the GB300 (sm_103a) paged GQA attention library.
+ *
+ * The operations follow the pages "Building Kshipra" part 3 (kshipra-3):
+ *  - section 1 "Block-Arena KV Cache": keys and values live in one arena of
+ *    fixed-size blocks reserved once; nothing is allocated per token.  KV
+ *    bytes per token = 2 x layers x KV heads x head dim x bytes per element.
+ *  - section 4 "Chunked Prefill": attention runs an online softmax (running
+ *    max, running sum, rescaled accumulator) across KV blocks read in place
+ *    from the arena, with no gather copy; RoPE uses absolute positions (a
+ *    chunk after P cached tokens starts at position P); the causal mask lets
+ *    each query see the cached prefix and the earlier tokens of its chunk.
+ *  - section 3 "Radix-Tree Prefix Cache": several block tables may name the
+ *    same physical blocks (shared prefixes); the kernels only read them.
+ *  - section 5 "Continuous Batching": one call may mix prefill chunks and
+ *    single-token decodes.
+ *
+ * Conventions for every entry point
+ *  - Pointers documented as "device" are CUDA device pointers owned by the
+ *    caller; the library never frees or keeps them past the call.  Pointers
+ *    documented as "host" are ordinary host memory.
+ *  - Calls that take a `stream` (a cudaStream_t passed as void*; NULL is the
+ *    legacy default stream) only enqueue work on it and return without
+ *    waiting, except kshipra_device_status, which waits for that stream.
+ *  - The library allocates no memory per call.  Scratch space is the
+ *    caller's `workspace`.
+ *  - The return value is a status code: KSHIPRA_OK or one of the errors
+ *    below.  Host-side checks run before anything is enqueued, so a call that
+ *    returns an argument error has touched no device memory.
+ *    kshipra_last_error() gives a one-line description of the last error
+ *    raised on the calling thread.
+ *  - Facts held only in device arrays (block ids inside [0, num_blocks),
+ *    positions consistent with context lengths, num_tokens ==
+ *    query_start_loc[num_seqs]) cannot be checked on the host.  They are
+ *    preconditions; kernels that meet a violation skip the offending access,
+ *    never trap, and set a bit in the device status word read by
+ *    kshipra_device_status.
+ *
+ * Layouts (element type `dtype`: 0 = IEEE binary16, 1 = bfloat16)
+ *  - token rows q, k, v, q_rot, out: [num_tokens][heads][head_dim], tokens of
+ *    sequence s contiguous in query_start_loc order.
+ *  - arena: k_arena and v_arena are each [num_blocks][num_kv_heads]
+ *    [block_size][head_dim]; slot p % block_size of logical block
+ *    p / block_size holds position p.
+ *  - block_tables: int32 [num_seqs][max_blocks_per_seq]; entry j of row s is
+ *    the physical block holding logical block j of sequence s.  Entries past
+ *    ceil(context_len / block_size) are never read.
+ *  - query q head h uses kv head h / (num_q_heads / num_kv_heads).
+ *
+ * Supported shapes: head_dim 64 or 128; block_size 16 or 32; num_q_heads /
+ * num_kv_heads in {1, 2, 4, 8, 16}; dtype 0 or 1.
+ */
+#ifndef KSHIPRA_H
+#define KSHIPRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define KSHIPRA_OK 0
+#define KSHIPRA_ERR_INVALID_ARG 1        /* null pointer, negative size, heads not divisible */
+#define KSHIPRA_ERR_UNSUPPORTED 2        /* head_dim, block_size, group size or dtype not built */
+#define KSHIPRA_ERR_WORKSPACE_TOO_SMALL 3
+#define KSHIPRA_ERR_CUDA 4               /* a CUDA call failed; see kshipra_last_error() */
+
+/* ---- device status word bits (kshipra_device_status) ----------------- */
+#define KSHIPRA_DEV_BAD_BLOCK_ID 0x1     /* a block-table entry outside [0, num_blocks) */
+#define KSHIPRA_DEV_BAD_POSITION 0x2     /* a position outside [0, rope_max_pos) or past the table */
+#define KSHIPRA_DEV_BAD_LENGTHS 0x4      /* context/query lengths inconsistent with the arguments */
+#define KSHIPRA_DEV_TIMEOUT 0x8          /* a bounded wait inside a kernel gave up */
+
+#define KSHIPRA_DTYPE_F16 0
+#define KSHIPRA_DTYPE_BF16 1
+
+/* ---- options (kshipra_set_option) ------------------------------------ */
+/* Keys per decode split (0 = automatic).  Nonzero values must be multiples
+ * of 64.  Process-wide; affects the workspace size. */
+#define KSHIPRA_OPT_SPLIT_TOKENS 0
+/* A sequence whose query_len x group size is at most this many rows runs on
+ * the split-KV decode kernel, all others on the tensor-core prefill kernel.
+ * 0..16, default 16; 0 sends every sequence to the prefill kernel. */
+#define KSHIPRA_OPT_DECODE_MAX_ROWS 1
+
+/*
+ * KV bytes one token occupies across all layers:
+ *   2 (K and V) x num_layers x num_kv_heads x head_dim x element size.
+ * (kshipra-3, section 1: 128 KiB per token for 32 layers, 8 KV heads, head
+ * dim 128, FP16.)  Host only.  Returns 0 for a non-positive argument or an
+ * unknown dtype.
+ */
+size_t kshipra_kv_bytes_per_token(int num_layers, int num_kv_heads, int head_dim, int dtype);
+
+/*
+ * RoPE table on the host: host_out[p][i][0] = cos(p * theta^(-2i/d)),
+ * host_out[p][i][1] = sin(...), for p < max_pos, i < head_dim / 2, in
+ * float64 (rotate-half convention: element i pairs with i + d/2).
+ * (kshipra-3, section 4: RoPE uses absolute positions.)  The caller copies it
+ * to the device once and passes that copy to kshipra_kv_append_rope.
+ * host_out must hold max_pos * head_dim entries.  Host only, no CUDA calls.
+ * Errors: INVALID_ARG (null, max_pos < 0, head_dim odd or < 2, theta <= 0).
+ */
+int kshipra_rope_table_build(double* host_out, int max_pos, int head_dim, double theta);
+
+/*
+ * RoPE and append (kshipra-3, sections 1 and 4).  For every token t of
+ * sequence s (query_start_loc[s] <= t < query_start_loc[s+1]) at position
+ * p = positions[t]:
+ *   - q_rot[t][h] = RoPE(q[t][h], p) for every q head (skipped when q and
+ *     q_rot are both NULL, e.g. when filling a cached prefix);
+ *   - k_arena[b][h][p % block_size] = RoPE(k[t][h], p) and
+ *     v_arena[b][h][p % block_size] = v[t][h] for every kv head, where
+ *     b = block_tables[s][p / block_size].
+ * The rotation is computed in float64 from rope_table (separate products,
+ * then one add) and rounded once to dtype (nearest, ties to even), so the
+ * arena contents are reproducible bit for bit.  V rows are copied bit for
+ * bit.  q_rot may alias q.  Other arena slots are not touched.
+ *
+ * q, q_rot [num_tokens][num_q_heads][head_dim]; k, v [num_tokens]
+ * [num_kv_heads][head_dim]; k_arena, v_arena, block_tables, query_start_loc
+ * [num_seqs + 1], positions [num_tokens], rope_table [rope_max_pos]
+ * [head_dim/2][2] float64: all device pointers.
+ * Device-side violations: a block id outside [0, num_blocks), a logical block
+ * index >= max_blocks_per_seq or a position outside [0, rope_max_pos) skip
+ * that token's writes and set KSHIPRA_DEV_BAD_BLOCK_ID / _BAD_POSITION.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA.  num_tokens == 0 is a no-op.
+ */
+int kshipra_kv_append_rope(const void* q, const void* k, const void* v, void* q_rot, void* k_arena,
+                           void* v_arena, const int32_t* block_tables, const int32_t* query_start_loc,
+                           const int32_t* positions, const double* rope_table, int rope_max_pos, int num_seqs,
+                           int num_tokens, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int max_blocks_per_seq, int num_blocks, int dtype, void* stream);
+
+/*
+ * Bytes of device workspace kshipra_paged_attention needs for these sizes,
+ * written to *bytes_out (host pointer).  sm_count is the number of SMs of the
+ * device the call will run on (0 = ask the current device, which needs a
+ * CUDA device).  The result depends on KSHIPRA_OPT_SPLIT_TOKENS.
+ * Errors: INVALID_ARG, CUDA (sm_count == 0 and no device).
+ */
+int kshipra_paged_attention_workspace_size(int num_seqs, int num_tokens, int max_context_len, int num_q_heads,
+                                           int num_kv_heads, int head_dim, int sm_count, size_t* bytes_out);
+
+/*
+ * Paged GQA attention over the arena (kshipra-3, section 4; mixed batches,
+ * section 5).  For every query token t of sequence s at position
+ * p = positions[t] and every q head h:
+ *   out[t][h] = sum_j softmax_j(scale * q_rot[t][h] . K_s[j]) V_s[j]
+ * over keys j = 0..p of sequence s, where K_s[j] / V_s[j] are read in place
+ * from the arena through block_tables (no gather copy).  Requires
+ * positions[t] < context_lens[s] and context_lens[s] <= max_context_len.
+ * Accumulation is float32; out is rounded once to dtype.
+ *
+ * Sequences with query_len x group <= KSHIPRA_OPT_DECODE_MAX_ROWS run on a
+ * split-KV decode kernel (partial results in `workspace`, then a combine
+ * pass); the others on a tcgen05 tensor-core chunked-prefill kernel with
+ * fully masked key tiles skipped.  The split is decided on the device, so
+ * one call may mix both kinds.
+ *
+ * out, q_rot [num_tokens][num_q_heads][head_dim]; k_arena, v_arena,
+ * block_tables, context_lens [num_seqs], query_start_loc [num_seqs + 1],
+ * positions [num_tokens], workspace: device pointers.  workspace must be
+ * 256-byte aligned and at least kshipra_paged_attention_workspace_size()
+ * bytes (it may be NULL when that size is 0).  out must not alias q_rot.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA.
+ */
+int kshipra_paged_attention(void* out, const void* q_rot, const void* k_arena, const void* v_arena,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            const int32_t* query_start_loc, const int32_t* positions, int num_seqs,
+                            int num_tokens, int max_query_len, int max_context_len, int num_q_heads,
+                            int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                            int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * Reads the current device's status word into *code_out (host pointer) and
+ * clears it, after waiting for `stream`.  0 means no kernel reported a
+ * violation since the last read.  Errors: INVALID_ARG, CUDA.
+ */
+int kshipra_device_status(int32_t* code_out, void* stream);
+
+/* Process-wide tuning switch (KSHIPRA_OPT_*).  Errors: INVALID_ARG. */
+int kshipra_set_option(int option, int value);
+
+/* Static description of a status code. */
+const char* kshipra_status_string(int code);
+
+/* One-line description of the last error on the calling thread ("" if none). */
+const char* kshipra_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KSHIPRA_H */

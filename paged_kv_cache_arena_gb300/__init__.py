@@ -1,0 +1,132 @@
+"""Paged GQA attention over a block-arena KV cache, for GB300 (sm_103a).
+
+Thin Python binding of the C ABI in ``include/kshipra.h``: each function has
+the C entry point's name, takes torch tensors for the device buffers, reads
+sizes off their shapes and passes raw pointers through ctypes.  All
+arithmetic runs in the library's CUDA kernels; nothing here computes.
+
+Pages "Building Kshipra" part 3 (kshipra-3): section 1 (block arena, KV bytes
+per token), section 4 (RoPE at absolute positions, online-softmax attention
+over in-place arena blocks, causal mask over the chunk), section 5 (mixed
+prefill/decode batches).
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import _lib
+
+KSHIPRA_OK = 0
+KSHIPRA_ERR_INVALID_ARG = 1
+KSHIPRA_ERR_UNSUPPORTED = 2
+KSHIPRA_ERR_WORKSPACE_TOO_SMALL = 3
+KSHIPRA_ERR_CUDA = 4
+
+KSHIPRA_DEV_BAD_BLOCK_ID = 0x1
+KSHIPRA_DEV_BAD_POSITION = 0x2
+KSHIPRA_DEV_BAD_LENGTHS = 0x4
+KSHIPRA_DEV_TIMEOUT = 0x8
+
+KSHIPRA_DTYPE_F16 = 0
+KSHIPRA_DTYPE_BF16 = 1
+
+KSHIPRA_OPT_SPLIT_TOKENS = 0
+KSHIPRA_OPT_DECODE_MAX_ROWS = 1
+
+
+class KshipraError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        lib = _lib.load()
+        msg = lib.kshipra_last_error().decode() or lib.kshipra_status_string(code).decode()
+        super().__init__("%s: %s (status %d)" % (where, msg, code))
+        self.code = code
+
+
+def _check(code: int, where: str) -> None:
+    if code != KSHIPRA_OK:
+        raise KshipraError(code, where)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    if t is None:
+        return ctypes.c_void_p(0)
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return KSHIPRA_DTYPE_F16
+    if t.dtype == torch.bfloat16:
+        return KSHIPRA_DTYPE_BF16
+    raise ValueError("unsupported tensor dtype %s" % t.dtype)
+
+
+def kshipra_kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int, dtype: int) -> int:
+    return int(_lib.load().kshipra_kv_bytes_per_token(num_layers, num_kv_heads, head_dim, dtype))
+
+
+def kshipra_rope_table_build(max_pos: int, head_dim: int, theta: float) -> np.ndarray:
+    """Host float64 table [max_pos, head_dim/2, 2] of (cos, sin)."""
+    out = np.empty((max_pos, head_dim // 2, 2), dtype=np.float64)
+    _check(_lib.load().kshipra_rope_table_build(ctypes.c_void_p(out.ctypes.data), max_pos, head_dim, float(theta)),
+           "kshipra_rope_table_build")
+    return out
+
+
+def kshipra_kv_append_rope(q, k, v, q_rot, k_arena, v_arena, block_tables, query_start_loc, positions,
+                           rope_table, stream=None) -> None:
+    """q/q_rot may be None (prefix fill).  Shapes as in include/kshipra.h."""
+    num_tokens, num_kv_heads, head_dim = k.shape
+    num_q_heads = q.shape[1] if q is not None else num_kv_heads
+    num_blocks, _, block_size, _ = k_arena.shape
+    _check(_lib.load().kshipra_kv_append_rope(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(q_rot), _ptr(k_arena), _ptr(v_arena), _ptr(block_tables),
+        _ptr(query_start_loc), _ptr(positions), _ptr(rope_table), rope_table.shape[0],
+        query_start_loc.shape[0] - 1, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
+        block_tables.shape[1], num_blocks, _dtype_code(k), _stream(stream)), "kshipra_kv_append_rope")
+
+
+def kshipra_paged_attention_workspace_size(num_seqs: int, num_tokens: int, max_context_len: int,
+                                           num_q_heads: int, num_kv_heads: int, head_dim: int,
+                                           sm_count: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.load().kshipra_paged_attention_workspace_size(num_seqs, num_tokens, max_context_len, num_q_heads,
+                                                              num_kv_heads, head_dim, sm_count, ctypes.byref(out)),
+           "kshipra_paged_attention_workspace_size")
+    return int(out.value)
+
+
+def kshipra_paged_attention(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc, positions,
+                            max_query_len: int, max_context_len: int, scale: float, workspace=None,
+                            stream=None) -> None:
+    num_tokens, num_q_heads, head_dim = q_rot.shape
+    num_blocks, num_kv_heads, block_size, _ = k_arena.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.load().kshipra_paged_attention(
+        _ptr(out), _ptr(q_rot), _ptr(k_arena), _ptr(v_arena), _ptr(block_tables), _ptr(context_lens),
+        _ptr(query_start_loc), _ptr(positions), query_start_loc.shape[0] - 1, num_tokens, max_query_len,
+        max_context_len, num_q_heads, num_kv_heads, head_dim, block_size, block_tables.shape[1], num_blocks,
+        float(scale), _dtype_code(q_rot), _ptr(workspace), ws_bytes, _stream(stream)), "kshipra_paged_attention")
+
+
+def kshipra_device_status(stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check(_lib.load().kshipra_device_status(ctypes.byref(code), _stream(stream)), "kshipra_device_status")
+    return int(code.value)
+
+
+def kshipra_set_option(option: int, value: int) -> None:
+    _check(_lib.load().kshipra_set_option(option, value), "kshipra_set_option")

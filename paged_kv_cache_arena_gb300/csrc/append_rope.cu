@@ -1,0 +1,117 @@
+// RoPE-and-append: rotates each new token's q and k at its absolute position
+// and writes rotated K and raw V into the token's arena slot.
+//
+// Pages "Building Kshipra" part 3 (kshipra-3): section 1 (the block arena:
+// the slot of position p is p % block_size in logical block p / block_size,
+// reached through the sequence's block table; nothing is allocated per token)
+// and section 4 (RoPE at absolute positions: a chunk after P cached tokens
+// starts at position P).
+//
+// One CTA per token.  The rotation is done in float64 from the caller's
+// (cos, sin) table with separate products and one add, then rounded once to
+// the storage type, so the arena image is reproducible bit for bit.  The
+// volume is small (num_tokens x (Hq + Hkv) x head_dim elements per call); the
+// kernel is memory-latency bound and far from the hot path's cost.
+#include "common.cuh"
+#include "internal.h"
+
+namespace kshipra {
+namespace {
+
+constexpr int kAppendThreads = 128;
+
+// Rotates pairs (i, i + d/2) and (i + 1, i + 1 + d/2) of one head row.
+template <bool kBf16>
+__device__ __forceinline__ void rotate_two_pairs(const uint16_t* src, uint16_t* dst, int i, int half,
+                                                 const double* cs) {
+  const uint32_t lo = *reinterpret_cast<const uint32_t*>(src + i);
+  const uint32_t hi = *reinterpret_cast<const uint32_t*>(src + i + half);
+  const double2 t01 = *reinterpret_cast<const double2*>(cs + 2 * i);      // c_i, s_i
+  const double2 t23 = *reinterpret_cast<const double2*>(cs + 2 * i + 2);  // c_i+1, s_i+1
+    const double x0 = bits_to_double<kBf16>(static_cast<uint16_t>(lo & 0xFFFF));
+  const double x1 = bits_to_double<kBf16>(static_cast<uint16_t>(lo >> 16));
+  const double y0 = bits_to_double<kBf16>(static_cast<uint16_t>(hi & 0xFFFF));
+  const double y1 = bits_to_double<kBf16>(static_cast<uint16_t>(hi >> 16));
+  const double a0 = __dsub_rn(__dmul_rn(x0, t01.x), __dmul_rn(y0, t01.y));
+  const double b0 = __dadd_rn(__dmul_rn(y0, t01.x), __dmul_rn(x0, t01.y));
+  const double a1 = __dsub_rn(__dmul_rn(x1, t23.x), __dmul_rn(y1, t23.y));
+  const double b1 = __dadd_rn(__dmul_rn(y1, t23.x), __dmul_rn(x1, t23.y));
+  const uint32_t olo = static_cast<uint32_t>(double_to_bits<kBf16>(a0)) |
+                       (static_cast<uint32_t>(double_to_bits<kBf16>(a1)) << 16);
+  const uint32_t ohi = static_cast<uint32_t>(double_to_bits<kBf16>(b0)) |
+                       (static_cast<uint32_t>(double_to_bits<kBf16>(b1)) << 16);
+  *reinterpret_cast<uint32_t*>(dst + i) = olo;
+  *reinterpret_cast<uint32_t*>(dst + i + half) = ohi;
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendArgs a) {
+  const int t = blockIdx.x;
+  if (t >= a.num_tokens) return;
+  // sequence of token t: the last s with query_start_loc[s] <= t
+  int lo = 0, hi = a.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.query_start_loc + mid) <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const int s = lo;
+  const int pos = __ldg(a.positions + t);
+  if (t < __ldg(a.query_start_loc + s) || t >= __ldg(a.query_start_loc + s + 1)) {  // outside every sequence
+    if (threadIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
+    return;
+  }
+  if (pos < 0 || pos >= a.rope_max_pos || pos / a.block_size >= a.max_blocks_per_seq) {
+    if (threadIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_POSITION);
+    return;
+  }
+  const int blk = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + pos / a.block_size);
+  const bool blk_ok = blk >= 0 && blk < a.num_blocks;
+  if (!blk_ok && threadIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
+  const int slot = pos % a.block_size;
+  const int D = a.head_dim, half = D / 2, pairs2 = half / 2;  // two pairs per work item
+  const double* cs = a.rope_table + static_cast<size_t>(pos) * D;  // [d/2][2] for this position
+
+  // q rows (optional)
+  if (a.q != nullptr) {
+    const uint16_t* qsrc = static_cast<const uint16_t*>(a.q) + static_cast<size_t>(t) * a.num_q_heads * D;
+    uint16_t* qdst = static_cast<uint16_t*>(a.q_rot) + static_cast<size_t>(t) * a.num_q_heads * D;
+    for (int w = threadIdx.x; w < a.num_q_heads * pairs2; w += blockDim.x) {
+      const int h = w / pairs2, i = 2 * (w % pairs2);
+      rotate_two_pairs<kBf16>(qsrc + h * D, qdst + h * D, i, half, cs);
+    }
+  }
+  if (!blk_ok) return;
+  // k rows -> arena, rotated
+  const uint16_t* ksrc = static_cast<const uint16_t*>(a.k) + static_cast<size_t>(t) * a.num_kv_heads * D;
+  uint16_t* karena = static_cast<uint16_t*>(a.k_arena);
+  for (int w = threadIdx.x; w < a.num_kv_heads * pairs2; w += blockDim.x) {
+    const int h = w / pairs2, i = 2 * (w % pairs2);
+    const size_t row = (static_cast<size_t>(blk) * a.num_kv_heads + h) * a.block_size + slot;
+    rotate_two_pairs<kBf16>(ksrc + h * D, karena + row * D, i, half, cs);
+  }
+  // v rows -> arena, bit copy in 16-byte pieces
+  const uint4* vsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) +
+                                                     static_cast<size_t>(t) * a.num_kv_heads * D);
+  uint16_t* varena = static_cast<uint16_t*>(a.v_arena);
+  const int vec_per_row = D / 8;
+  for (int w = threadIdx.x; w < a.num_kv_heads * vec_per_row; w += blockDim.x) {
+    const int h = w / vec_per_row, c = w % vec_per_row;
+    const size_t row = (static_cast<size_t>(blk) * a.num_kv_heads + h) * a.block_size + slot;
+    reinterpret_cast<uint4*>(varena + row * D)[c] = vsrc[w];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append_rope(const AppendArgs& a, cudaStream_t stream) {
+  if (a.num_tokens == 0) return cudaSuccess;
+  dim3 grid(a.num_tokens), block(kAppendThreads);
+  if (a.dtype == KSHIPRA_DTYPE_BF16)
+    append_rope_kernel<true><<<grid, block, 0, stream>>>(a);
+  else
+    append_rope_kernel<false><<<grid, block, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kshipra

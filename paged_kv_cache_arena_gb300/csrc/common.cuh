@@ -1,0 +1,250 @@
+// Shared device helpers for the sm_103a kernels: shared-memory barriers, TMA
+// loads, warp-level matrix loads / MMA, tcgen05 (TMEM) wrappers, IEEE
+// rounding from double, and the device status word.  Inline PTX written from
+// the PTX ISA; no library kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "../../include/kshipra.h"
+
+namespace kshipra {
+
+// ---------------------------------------------------------------- status
+
+// Nanoseconds a bounded wait may spin before it reports KSHIPRA_DEV_TIMEOUT.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ void report(unsigned* status, unsigned bit) {
+  if (status) atomicOr(status, bit);
+}
+
+__device__ __forceinline__ bool timed_out_globally(const unsigned* status) {
+  return (*(volatile const unsigned*)status & KSHIPRA_DEV_TIMEOUT) != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Gives up after
+// kWaitLimitNs (or at once if another CTA already timed out), sets
+// KSHIPRA_DEV_TIMEOUT and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs || timed_out_globally(status)) {
+      report(status, KSHIPRA_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- TMA
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Make generic-proxy writes to shared memory visible to the async proxy
+// (TMA, tensor cores).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- warp MMA
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (kBf16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+// 2^x on the special-function unit.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (kBf16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint16_t round_f32(float x) {
+  if constexpr (kBf16) {
+    __nv_bfloat16 v = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t*>(&v);
+  } else {
+    __half v = __float2half_rn(x);
+    return *reinterpret_cast<uint16_t*>(&v);
+  }
+}
+
+// ---------------------------------------------------------------- IEEE
+
+// Storage bits -> double (exact).
+template <bool kBf16>
+__device__ __forceinline__ double bits_to_double(uint16_t h) {
+  if constexpr (kBf16) {
+    return static_cast<double>(__uint_as_float(static_cast<uint32_t>(h) << 16));
+  } else {
+    return static_cast<double>(__half2float(__ushort_as_half(h)));
+  }
+}
+
+// double -> storage bits with a single rounding (nearest, ties to even),
+// written with integer operations on the IEEE encoding.  EB exponent bits,
+// MB fraction bits of the target format.
+template <int EB, int MB>
+__device__ __forceinline__ uint16_t double_to_small(double x) {
+  const uint64_t b = static_cast<uint64_t>(__double_as_longlong(x));
+  const uint32_t sign = static_cast<uint32_t>(b >> 63) << (EB + MB);
+  const uint64_t mag = b & 0x7FFFFFFFFFFFFFFFull;
+  constexpr int kExpAllOnes = (1 << EB) - 1;
+  constexpr int kBias = (1 << (EB - 1)) - 1;
+  if (mag >= 0x7FF0000000000000ull) {  // infinity or NaN
+    const uint32_t frac = mag > 0x7FF0000000000000ull ? (1u << (MB - 1)) : 0u;
+    return static_cast<uint16_t>(sign | (kExpAllOnes << MB) | frac);
+  }
+  const int dexp = static_cast<int>(mag >> 52);
+  if (dexp == 0) return static_cast<uint16_t>(sign);  // zero / double subnormal
+  const int texp = dexp - 1023 + kBias;               // biased exponent in the target
+  if (texp >= kExpAllOnes) return static_cast<uint16_t>(sign | (kExpAllOnes << MB));
+  const uint64_t sig = (mag & 0x000FFFFFFFFFFFFFull) | 0x0010000000000000ull;
+  const int drop = texp >= 1 ? 52 - MB : 52 - MB + 1 - texp;  // low bits removed
+  if (drop >= 54) return static_cast<uint16_t>(sign);
+  uint64_t kept = sig >> drop;
+  const uint64_t rest = sig & ((1ull << drop) - 1);
+  const uint64_t halfway = 1ull << (drop - 1);
+  kept += (rest > halfway || (rest == halfway && (kept & 1))) ? 1 : 0;
+  // normal: kept still holds the hidden bit, so (texp - 1) << MB + kept adds
+  // it into the exponent field; a rounding carry moves up one binade.
+  const uint64_t enc = texp >= 1 ? (static_cast<uint64_t>(texp - 1) << MB) + kept : kept;
+  return static_cast<uint16_t>(sign | static_cast<uint32_t>(enc));
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint16_t double_to_bits(double x) {
+  if constexpr (kBf16)
+    return double_to_small<8, 7>(x);
+  else
+    return double_to_small<5, 10>(x);
+}
+
+// ---------------------------------------------------------------- host
+
+// Raises a kernel's dynamic shared-memory limit once per device.
+template <typename Kernel>
+inline cudaError_t set_smem_limit_once(Kernel* kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+}  // namespace kshipra

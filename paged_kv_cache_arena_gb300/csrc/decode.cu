@@ -1,0 +1,411 @@
+// Split-KV decode attention over the block arena, and the split-combine pass.
+//
+// Pages "Building Kshipra" part 3 (kshipra-3), section 4: attention runs an
+// online softmax (running max m, running sum l, rescaled accumulator o) over
+// KV blocks read in place from the arena, and the merge is exact, so the key
+// range of one sequence can be cut into splits whose partial (m, l, o) are
+// merged afterwards with the same rescaling rule.  Section 1: keys of
+// position p sit in slot p % block_size of physical block
+// block_tables[s][p / block_size].
+//
+// Work unit (one CTA): (sequence s, kv head h, split).  All query rows that
+// share kv head h -- query_len x group rows, at most 16 -- are served from one
+// read of each K/V tile.
+//  - Each of the 4 warps owns every 4th 16-key chunk of the split and keeps a
+//    3-deep ring of shared-memory stages.  Lane 0 fills a stage with four TMA
+//    tile loads (K and V, two 64-column halves each, 128-byte swizzle)
+//    straight from the arena block, completing on the stage's mbarrier.
+//  - Scores are computed as S^T = K q^T with mma.sync m16n8k16 (keys on the
+//    16-row side, query rows on the 8-column side), so no query padding to 16
+//    rows is needed; fp32 accumulation.
+//  - Online softmax in registers with quad-lane shuffles for the row max; the
+//    running sum stays per lane until the end.
+//  - P^T is turned into the B operand of O^T = V^T P^T with movmatrix, V^T
+//    comes from ldmatrix.trans; keys past the context (possibly NaN) get
+//    zeroed value rows.
+//  - Warps merge through shared memory; a single-split sequence writes its
+//    rounded output directly, otherwise the partial (m, l, o) goes to the
+//    workspace and combine_kernel merges the splits.
+#include <float.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kshipra {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;
+constexpr int kChunk = 16;  // keys per stage
+constexpr float kNegInf = -INFINITY;
+
+template <int D>
+struct DecodeLayout {
+  static constexpr int kRegions = D / 64;                      // 64-column swizzle regions
+  static constexpr int kRegionBytes = kChunk * 128;            // 16 rows x 128 B
+  static constexpr int kTileBytes = kRegions * kRegionBytes;   // K (or V) of one chunk
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kWarpBytes = kStages * kStageBytes;
+  static constexpr int kBarOffset = kWarps * kWarpBytes;
+  static constexpr int kBytes = kBarOffset + kWarps * kStages * 8;
+  static constexpr int kMergeBytes = kWarps * (2 * 16 + 16 * D) * 4;
+  static_assert(kMergeBytes <= kBarOffset, "merge scratch must fit in the stage buffers");
+  static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+template <int D, bool kBf16, int NT>
+__device__ __forceinline__ void decode_body(const CUtensorMap* kmap, const CUtensorMap* vmap, const AttnArgs& a,
+                                            uint8_t* smem, int s, int h, int split, int q0, int nrows, int ctx,
+                                            int nsplit) {
+  using L = DecodeLayout<D>;
+  constexpr int KS = D / 16;  // 16-wide steps over the head dimension
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int G = a.group;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOffset) + warp * kStages;
+  uint8_t* wbase = smem + warp * L::kWarpBytes;
+
+  const int tok_begin = split * a.split_tokens;
+  const int tok_end = min(ctx, tok_begin + a.split_tokens);
+  const int nchunks = ceil_div(tok_end - tok_begin, kChunk);
+  const int my_chunks = nchunks > warp ? ceil_div(nchunks - warp, kWarps) : 0;
+  const int oob_row = a.num_blocks * a.num_kv_heads * a.block_size;  // past the tensor: zero fill
+
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  auto issue = [&](int i) {  // lane 0 only: load this warp's i-th chunk
+    const int c = warp + kWarps * i;
+    const int tok = tok_begin + c * kChunk;
+    const int blk = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + tok / a.block_size);
+    int row;
+    if (blk < 0 || blk >= a.num_blocks) {
+      report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
+      row = oob_row;
+    } else {
+      row = (blk * a.num_kv_heads + h) * a.block_size + (tok % a.block_size);
+    }
+    uint8_t* stg = wbase + (i % kStages) * L::kStageBytes;
+    uint64_t* bar = &bars[i % kStages];
+    mbar_arrive_expect_tx(bar, L::kStageBytes);
+#pragma unroll
+    for (int r = 0; r < L::kRegions; ++r) {
+      tma_load_2d(stg + r * L::kRegionBytes, kmap, 64 * r, row, bar);
+      tma_load_2d(stg + L::kTileBytes + r * L::kRegionBytes, vmap, 64 * r, row, bar);
+    }
+  };
+  int issued = 0;
+  if (lane == 0) {
+    for (; issued < min(kStages, my_chunks); ++issued) issue(issued);
+  }
+
+  // Query fragments: B operand of S^T = K q^T.  Column n of n-tile nt is
+  // query row 8 nt + g = (token q0 + n / G, q head h G + n % G).
+  uint32_t qb[NT][KS][2];
+  int rpos[NT][2];
+  const uint16_t* qrot = static_cast<const uint16_t*>(a.q_rot);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int n = 8 * nt + g;
+    const uint16_t* qp = nullptr;
+    if (n < nrows)
+      qp = qrot + (static_cast<size_t>(q0 + n / G) * a.num_q_heads + h * G + n % G) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qb[nt][ks][0] = qp ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * t4)) : 0u;
+      qb[nt][ks][1] = qp ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8 + 2 * t4)) : 0u;
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = 8 * nt + 2 * t4 + e;
+      rpos[nt][e] = r < nrows ? __ldg(a.positions + q0 + r / G) : -1;
+    }
+  }
+
+  float m[NT][2], l[NT][2], o[NT][KS][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      m[nt][e] = kNegInf;
+      l[nt][e] = 0.f;
+    }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[nt][mt][k] = 0.f;
+  }
+  const float c2 = a.scale_log2;
+  bool ok = true;
+  int consumed = 0;
+
+  for (int i = 0; i < my_chunks; ++i) {
+    const int st = i % kStages;
+    if (!mbar_wait(&bars[st], (i / kStages) & 1, a.status)) {
+      ok = false;
+      break;
+    }
+    consumed = i + 1;
+    const uint32_t kb = smem_u32(wbase + st * L::kStageBytes);
+    const uint32_t vb = kb + L::kTileBytes;
+    const int tok0 = tok_begin + (warp + kWarps * i) * kChunk;
+
+    // S^T (16 keys x 8 query rows per n-tile)
+    float sacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sacc[nt][k] = 0.f;
+    {
+      const int row = (lane & 7) + 8 * ((lane >> 3) & 1);
+      const uint32_t rbase = kb + row * 128;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int ch = 2 * (ks & 3) + (lane >> 4);
+        uint32_t af[4];
+        ldsm_x4(rbase + (ks >> 2) * L::kRegionBytes + ((ch ^ (row & 7)) << 4), af);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816<kBf16>(sacc[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
+      }
+    }
+
+    // causal mask (key j visible iff j <= the row's position) and online softmax
+    const int j0 = tok0 + g, j1 = j0 + 8;
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float s0 = j0 <= rpos[nt][e] ? sacc[nt][e] : kNegInf;
+        const float s1 = j1 <= rpos[nt][e] ? sacc[nt][e + 2] : kNegInf;
+        float mx = fmaxf(s0, s1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mnew = fmaxf(m[nt][e], mx);
+        const float ms = (mnew == kNegInf ? 0.f : mnew) * c2;
+        const float alpha = ex2(fmaf(m[nt][e], c2, -ms));
+        p[e] = ex2(fmaf(s0, c2, -ms));
+        p[e + 2] = ex2(fmaf(s1, c2, -ms));
+        l[nt][e] = fmaf(l[nt][e], alpha, p[e] + p[e + 2]);
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          o[nt][mt][e] *= alpha;
+          o[nt][mt][e + 2] *= alpha;
+        }
+        m[nt][e] = mnew;
+      }
+      pb[nt][0] = movmatrix_trans(pack2<kBf16>(p[0], p[1]));
+      pb[nt][1] = movmatrix_trans(pack2<kBf16>(p[2], p[3]));
+    }
+
+    // O^T (head dim x query rows) += V^T P^T
+    const bool tail = tok0 + kChunk > ctx;
+    uint32_t vmask_a = 0xFFFFFFFFu, vmask_b = 0xFFFFFFFFu;
+    if (tail) {  // value rows of keys past the context may hold anything
+      const int ta = tok0 + 2 * t4, tb = ta + 8;
+      vmask_a = (ta < ctx ? 0x0000FFFFu : 0u) | (ta + 1 < ctx ? 0xFFFF0000u : 0u);
+      vmask_b = (tb < ctx ? 0x0000FFFFu : 0u) | (tb + 1 < ctx ? 0xFFFF0000u : 0u);
+    }
+    {
+      const int row = (lane & 7) + 8 * (lane >> 4);
+      const uint32_t rbase = vb + row * 128;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const int ch = 2 * mt + ((lane >> 3) & 1);
+        uint32_t vf[4];
+        ldsm_x4_trans(rbase + (ch >> 3) * L::kRegionBytes + (((ch & 7) ^ (row & 7)) << 4), vf);
+        vf[0] &= vmask_a;
+        vf[1] &= vmask_a;
+        vf[2] &= vmask_b;
+        vf[3] &= vmask_b;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816<kBf16>(o[nt][mt], vf, pb[nt][0], pb[nt][1]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && issued < my_chunks) issue(issued++);
+  }
+
+  if (!ok) {
+    // a wait gave up: let this warp's outstanding loads land before the CTA
+    // reuses or releases its shared memory
+    if (lane == 0)
+      for (int i = consumed; i < issued; ++i) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&bars[i % kStages], (i / kStages) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        }
+      }
+    __syncwarp();
+  }
+
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float v = l[nt][e];
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      l[nt][e] = v;
+    }
+
+  __syncthreads();  // every warp's stages are drained: reuse them for the merge
+  const bool any_fail = __syncthreads_or(!ok);
+  float* mbuf = reinterpret_cast<float*>(smem);
+  float* lbuf = mbuf + kWarps * 16;
+  float* obuf = lbuf + kWarps * 16;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = 8 * nt + 2 * t4 + e;
+      if (g == 0) {
+        mbuf[warp * 16 + r] = m[nt][e];
+        lbuf[warp * 16 + r] = l[nt][e];
+      }
+      float* orow = obuf + (warp * 16 + r) * D;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        orow[16 * mt + g] = o[nt][mt][e];
+        orow[16 * mt + g + 8] = o[nt][mt][e + 2];
+      }
+    }
+  __syncthreads();
+  if (any_fail) return;
+
+  for (int idx = threadIdx.x; idx < nrows * D; idx += kThreads) {
+    const int r = idx / D, d = idx % D;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mbuf[w * 16 + r]);
+    float Lsum = 0.f, O = 0.f;
+    if (M != kNegInf) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = mbuf[w * 16 + r];
+        const float f = mw == kNegInf ? 0.f : ex2((mw - M) * c2);
+        Lsum = fmaf(lbuf[w * 16 + r], f, Lsum);
+        O = fmaf(obuf[(w * 16 + r) * D + d], f, O);
+      }
+    }
+    const int tok = q0 + r / G, head = h * G + r % G;
+    const size_t orow = static_cast<size_t>(tok) * a.num_q_heads + head;
+    if (nsplit == 1) {
+      static_cast<uint16_t*>(a.out)[orow * D + d] = round_f32<kBf16>(O / Lsum);
+    } else {
+      const size_t prow = static_cast<size_t>(split) * a.num_tokens * a.num_q_heads + orow;
+      a.ws_o[prow * D + d] = O;
+      if (d == 0) {
+        a.ws_ml[prow * 2] = M;
+        a.ws_ml[prow * 2 + 1] = Lsum;
+      }
+    }
+  }
+}
+
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                  const AttnArgs a) {
+  const int split = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int q0 = __ldg(a.query_start_loc + s);
+  const int qlen = __ldg(a.query_start_loc + s + 1) - q0;
+  const int nrows = qlen * a.group;
+  if (q0 < 0 || q0 + qlen > a.num_tokens) {  // query_start_loc inconsistent with num_tokens
+    if (split == 0 && h == 0 && threadIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
+    return;
+  }
+  if (qlen <= 0 || nrows > a.decode_max_rows) return;  // empty, or handled by the prefill kernel
+  const int ctx = __ldg(a.context_lens + s);
+  const int nsplit = ceil_div(ctx, a.split_tokens);
+  if (ctx <= 0 || ctx > a.max_blocks_per_seq * a.block_size || nsplit > a.max_splits) {
+    if (split == 0 && threadIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
+    return;
+  }
+  if (split >= nsplit) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (nrows <= 8)
+    decode_body<D, kBf16, 1>(&kmap, &vmap, a, smem, s, h, split, q0, nrows, ctx, nsplit);
+  else
+    decode_body<D, kBf16, 2>(&kmap, &vmap, a, smem, s, h, split, q0, nrows, ctx, nsplit);
+}
+
+// Merges the per-split partials of multi-split decode sequences:
+//   M = max_i m_i,  L = sum_i l_i 2^{(m_i - M) c},  out = sum_i o_i 2^{(m_i - M) c} / L.
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
+  const int h = blockIdx.x, s = blockIdx.y;
+  const int q0 = __ldg(a.query_start_loc + s);
+  const int qlen = __ldg(a.query_start_loc + s + 1) - q0;
+  const int nrows = qlen * a.group;
+  if (q0 < 0 || q0 + qlen > a.num_tokens || qlen <= 0 || nrows > a.decode_max_rows) return;
+  const int ctx = __ldg(a.context_lens + s);
+  const int nsplit = ceil_div(ctx, a.split_tokens);
+  if (nsplit <= 1 || nsplit > a.max_splits || ctx > a.max_blocks_per_seq * a.block_size) return;
+  const float c2 = a.scale_log2;
+  const size_t split_stride = static_cast<size_t>(a.num_tokens) * a.num_q_heads;
+  for (int idx = threadIdx.x; idx < nrows * D; idx += blockDim.x) {
+    const int r = idx / D, d = idx % D;
+    const int tok = q0 + r / a.group, head = h * a.group + r % a.group;
+    const size_t orow = static_cast<size_t>(tok) * a.num_q_heads + head;
+    float M = kNegInf;
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, a.ws_ml[(sp * split_stride + orow) * 2]);
+    float Lsum = 0.f, O = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const size_t prow = sp * split_stride + orow;
+      const float mi = a.ws_ml[prow * 2];
+      const float f = mi == kNegInf ? 0.f : ex2((mi - M) * c2);
+      Lsum = fmaf(a.ws_ml[prow * 2 + 1], f, Lsum);
+      O = fmaf(a.ws_o[prow * D + d], f, O);
+    }
+    static_cast<uint16_t*>(a.out)[orow * D + d] = round_f32<kBf16>(O / Lsum);
+  }
+}
+
+template <int D, bool kBf16>
+cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            cudaStream_t stream) {
+  using L = DecodeLayout<D>;
+  static std::atomic<unsigned long long> configured{0};
+  cudaError_t e = set_smem_limit_once(decode_kernel<D, kBf16>, L::kAlloc, configured);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.max_splits, a.num_kv_heads, a.num_seqs);
+  decode_kernel<D, kBf16><<<grid, kThreads, L::kAlloc, stream>>>(kmap, vmap, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t stream) {
+  if (a.num_seqs == 0 || a.decode_max_rows == 0) return cudaSuccess;
+  const bool bf = a.dtype == KSHIPRA_DTYPE_BF16;
+  if (a.head_dim == 128)
+    return bf ? launch_decode_t<128, true>(a, kmap, vmap, stream) : launch_decode_t<128, false>(a, kmap, vmap, stream);
+  return bf ? launch_decode_t<64, true>(a, kmap, vmap, stream) : launch_decode_t<64, false>(a, kmap, vmap, stream);
+}
+
+cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0 || a.decode_max_rows == 0 || a.max_splits <= 1) return cudaSuccess;
+  dim3 grid(a.num_kv_heads, a.num_seqs);
+  const bool bf = a.dtype == KSHIPRA_DTYPE_BF16;
+  if (a.head_dim == 128) {
+    if (bf) combine_kernel<128, true><<<grid, 128, 0, stream>>>(a);
+    else combine_kernel<128, false><<<grid, 128, 0, stream>>>(a);
+  } else {
+    if (bf) combine_kernel<64, true><<<grid, 128, 0, stream>>>(a);
+    else combine_kernel<64, false><<<grid, 128, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kshipra

@@ -1,0 +1,63 @@
+// Host-side interfaces between the C-ABI layer (api.cu) and the kernel
+// translation units.  Every launcher enqueues on `stream` and returns the
+// cudaError_t of the launch.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kshipra {
+
+// Rows of (token, q head) a decode unit handles at most: query_len x group.
+constexpr int kDecodeMaxRows = 16;
+
+struct AppendArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* q_rot;
+  void* k_arena;
+  void* v_arena;
+  const int32_t* block_tables;
+  const int32_t* query_start_loc;
+  const int32_t* positions;
+  const double* rope_table;
+  int rope_max_pos;
+  int num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks;
+  int dtype;
+  unsigned* status;
+};
+
+cudaError_t launch_append_rope(const AppendArgs& a, cudaStream_t stream);
+
+// Shared by the decode, combine and prefill kernels.
+struct AttnArgs {
+  void* out;
+  const void* q_rot;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start_loc;
+  const int32_t* positions;
+  float* ws_o;   // [max_splits][num_tokens][num_q_heads][head_dim] partial accumulators
+  float* ws_ml;  // [max_splits][num_tokens][num_q_heads][2] partial (max, sum)
+  unsigned* status;
+  int num_seqs, num_tokens, max_query_len, max_context_len;
+  int num_q_heads, num_kv_heads, group, head_dim, block_size, max_blocks_per_seq, num_blocks;
+  int split_tokens, max_splits;  // decode split size (keys) and count bound
+  int decode_max_rows;           // query_len * group at or below this -> decode kernel
+  float scale_log2;              // scale * log2(e)
+  int dtype;
+};
+
+// Split-KV decode (mma.sync on staged TMA tiles) followed by the combine pass.
+cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          cudaStream_t stream);
+cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream);
+
+// Chunked prefill on tcgen05 / TMEM.
+cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           const CUtensorMap& qmap, cudaStream_t stream);
+
+}  // namespace kshipra

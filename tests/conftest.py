@@ -17,3 +17,26 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def gpu():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    import paged_kv_cache_arena_gb300 as K
+    K.kshipra_device_status()  # clear anything left over
+    return K
+
+
+@pytest.fixture
+def clean_status(gpu):
+    """Fails a test that leaves a device status bit set; resets options."""
+    yield gpu
+    code = gpu.kshipra_device_status()
+    gpu.kshipra_set_option(gpu.KSHIPRA_OPT_SPLIT_TOKENS, 0)
+    gpu.kshipra_set_option(gpu.KSHIPRA_OPT_DECODE_MAX_ROWS, 16)
+    assert code == 0, "device status word 0x%x" % code

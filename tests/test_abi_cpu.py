@@ -1,0 +1,152 @@
+"""C-ABI checks that need no GPU: exports, host-only entry points, and the
+argument validation that must reject bad calls before any CUDA work."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kshipra.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_kv_cache_arena_gb300 import _lib
+    return _lib.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(kshipra_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    from paged_kv_cache_arena_gb300 import _lib
+    assert declared_symbols() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from paged_kv_cache_arena_gb300 import _lib
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (kshipra_\w+)", out))
+    for name in declared_symbols():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_kv_bytes_per_token_matches_the_pages(lib):
+    # kshipra-3 section 1: 128 KiB / 512 KiB per token, 512 MiB vs 2 GiB at 4096 tokens
+    rows = [l.split() for l in open(os.path.join(ROOT, "tests", "golden", "kv_bytes.txt"))
+            if l.strip() and not l.startswith("#")]
+    for layers, heads, hd, be, tokens, expected in (map(int, r) for r in rows):
+        assert be == 2
+        assert lib.kshipra_kv_bytes_per_token(layers, heads, hd, 0) * tokens == expected
+        assert lib.kshipra_kv_bytes_per_token(layers, heads, hd, 1) * tokens == expected
+    assert lib.kshipra_kv_bytes_per_token(0, 8, 128, 0) == 0
+    assert lib.kshipra_kv_bytes_per_token(32, 8, 128, 7) == 0
+
+
+def test_rope_table_equals_oracle_table(lib, oracle_mod):
+    import paged_kv_cache_arena_gb300 as K
+    for max_pos, d, theta in [(100, 64, 1.0e4), (5000, 128, 5.0e5), (1, 128, 5.0e5)]:
+        got = K.kshipra_rope_table_build(max_pos, d, theta)
+        ref = oracle_mod.rope_table(max_pos, d, theta)
+        assert np.array_equal(got, ref)  # same definition, both float64 libm
+
+
+def test_rope_table_rejects_bad_arguments(lib):
+    buf = np.zeros(16)
+    p = ctypes.c_void_p(buf.ctypes.data)
+    assert lib.kshipra_rope_table_build(None, 4, 4, 1e4) == 1
+    assert lib.kshipra_rope_table_build(p, -1, 4, 1e4) == 1
+    assert lib.kshipra_rope_table_build(p, 4, 3, 1e4) == 1
+    assert lib.kshipra_rope_table_build(p, 4, 4, 0.0) == 1
+    assert lib.kshipra_rope_table_build(p, 0, 4, 1e4) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+
+
+def append_args(**over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, q_rot=FAKE, k_arena=FAKE, v_arena=FAKE, bt=FAKE, qsl=FAKE, pos=FAKE,
+             table=FAKE, rope_max_pos=64, num_seqs=1, num_tokens=1, hq=4, hkv=2, d=64, bs=16, maxb=4, nb=16,
+             dtype=0, stream=None)
+    a.update(over)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(num_seqs=-1), 1), (dict(num_tokens=-1), 1), (dict(num_seqs=0), 1), (dict(hq=5), 1), (dict(hkv=0), 1),
+    (dict(hq=48, hkv=2), 2), (dict(d=96), 2), (dict(bs=8), 2), (dict(dtype=2), 2), (dict(nb=0), 1),
+    (dict(maxb=0), 1), (dict(q=None), 1), (dict(k=None), 1), (dict(bt=None), 1), (dict(table=None), 1),
+    (dict(rope_max_pos=0), 1), (dict(k_arena=ctypes.c_void_p(0x10008)), 1),
+    (dict(nb=1 << 26, hkv=8, hq=8), 2),
+])
+def test_append_validation(lib, over, code):
+    assert lib.kshipra_kv_append_rope(*append_args(**over)) == code
+    assert lib.kshipra_last_error()
+
+
+def test_append_with_no_tokens_is_a_noop(lib):
+    assert lib.kshipra_kv_append_rope(*append_args(num_tokens=0, num_seqs=0)) == 0
+
+
+def attn_args(**over):
+    a = dict(out=FAKE, q_rot=ctypes.c_void_p(0x20000), k_arena=FAKE, v_arena=FAKE, bt=FAKE, ctx=FAKE, qsl=FAKE,
+             pos=FAKE, num_seqs=1, num_tokens=1, max_q=1, max_ctx=10, hq=4, hkv=2, d=64, bs=16, maxb=4, nb=16,
+             scale=0.125, dtype=0, ws=None, ws_bytes=0, stream=None)
+    a.update(over)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(num_seqs=-1), 1), (dict(num_seqs=0), 1), (dict(max_ctx=0), 1), (dict(max_q=0), 1),
+    (dict(max_ctx=65), 1), (dict(hq=6, hkv=4), 1), (dict(hq=24, hkv=1), 2), (dict(d=256), 2), (dict(bs=64), 2),
+    (dict(dtype=-1), 2), (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(out=None), 1),
+    (dict(ctx=None), 1), (dict(q_rot=FAKE), 1), (dict(v_arena=ctypes.c_void_p(0x10004)), 1),
+])
+def test_attention_validation(lib, over, code):
+    assert lib.kshipra_paged_attention(*attn_args(**over)) == code
+
+
+def test_attention_with_no_tokens_is_a_noop(lib):
+    assert lib.kshipra_paged_attention(*attn_args(num_tokens=0, num_seqs=0)) == 0
+
+
+def test_workspace_size_host_only(lib):
+    import paged_kv_cache_arena_gb300 as K
+    # a short context needs one split: no partials
+    assert K.kshipra_paged_attention_workspace_size(4, 4, 100, 32, 8, 128, sm_count=152) == 0
+    big = K.kshipra_paged_attention_workspace_size(16, 16, 32768, 32, 8, 128, sm_count=152)
+    assert big > 0 and big % 256 == 0
+    K.kshipra_set_option(K.KSHIPRA_OPT_SPLIT_TOKENS, 1024)
+    try:
+        ws = K.kshipra_paged_attention_workspace_size(16, 16, 32768, 32, 8, 128, sm_count=152)
+        splits = 32
+        assert ws == -(-splits * 16 * 32 * 128 * 4 // 256) * 256 + -(-splits * 16 * 32 * 2 * 4 // 256) * 256
+    finally:
+        K.kshipra_set_option(K.KSHIPRA_OPT_SPLIT_TOKENS, 0)
+    out = ctypes.c_size_t(0)
+    assert lib.kshipra_paged_attention_workspace_size(1, 1, 10, 0, 1, 64, 152, ctypes.byref(out)) == 1
+    assert lib.kshipra_paged_attention_workspace_size(1, 1, 10, 4, 1, 64, 152, None) == 1
+
+
+def test_options_validation(lib):
+    assert lib.kshipra_set_option(0, 100) == 1
+    assert lib.kshipra_set_option(0, -64) == 1
+    assert lib.kshipra_set_option(1, 17) == 1
+    assert lib.kshipra_set_option(9, 0) == 1
+    assert lib.kshipra_set_option(0, 0) == 0
+    assert lib.kshipra_set_option(1, 16) == 0
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.kshipra_status_string(code)
+    assert lib.kshipra_status_string(99) == b"unknown status"

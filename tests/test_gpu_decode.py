@@ -1,0 +1,113 @@
+"""Split-KV decode attention on the GPU against the float64 oracle (pages
+"Building Kshipra" part 3, section 4: online softmax over in-place arena
+blocks; section 1: blocks reached through block tables)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, custom, random_decode
+from workloads import make_config
+from workloads.device import DeviceWorkload, bits_of
+
+pytestmark = pytest.mark.gpu
+
+
+def run(w, K=None, split=None, max_rows=None):
+    import paged_kv_cache_arena_gb300 as KK
+    if split is not None:
+        KK.kshipra_set_option(KK.KSHIPRA_OPT_SPLIT_TOKENS, split)
+    if max_rows is not None:
+        KK.kshipra_set_option(KK.KSHIPRA_OPT_DECODE_MAX_ROWS, max_rows)
+    dw = DeviceWorkload(w)
+    dw.step()
+    torch.cuda.synchronize()
+    return dw
+
+
+CASES = {
+    # several 16-key chunks per warp, ragged tails, several splits
+    "llama-shape": lambda: random_decode(1, 8, 17, 700),
+    "bs32-bf16": lambda: random_decode(2, 6, 1, 900, bs=32, dtype="bf16"),
+    "d64": lambda: random_decode(3, 5, 30, 500, Hq=16, Hkv=4, d=64),
+    "g1": lambda: random_decode(4, 4, 100, 400, Hq=8, Hkv=8),
+    "g2": lambda: random_decode(5, 4, 100, 400, Hq=8, Hkv=4),
+    "g8": lambda: random_decode(6, 4, 100, 400, Hq=16, Hkv=2),
+    "g16": lambda: random_decode(7, 3, 100, 400, Hq=32, Hkv=2, bs=32),
+    # several query tokens per sequence that still fit the decode kernel
+    "qlen2-g4": lambda: custom(8, prefix=[50, 300, 0], qlen=[2, 4, 3]),
+    "qlen2-g8-bf16": lambda: custom(9, Hq=16, Hkv=2, dtype="bf16", prefix=[77, 5], qlen=[2, 2]),
+    "ctx1": lambda: custom(10, prefix=[0, 0, 1], qlen=[1, 1, 1]),
+}
+
+
+@pytest.mark.parametrize("split", [None, 64, 192])
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_decode_matches_oracle(clean_status, name, split):
+    w = CASES[name]()
+    dw = run(w, split=split)
+    assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype, name)
+
+
+def test_single_key_returns_its_value_exactly(clean_status):
+    w = custom(11, Hq=8, Hkv=2, prefix=[0, 0], qlen=[1, 1])
+    dw = run(w)
+    v0 = bits_of(dw.v_new)  # the only key of each sequence is the new token
+    got = bits_of(dw.out).reshape(2, 2, 4, -1)
+    for s in range(2):
+        for g in range(4):
+            assert np.array_equal(got[s, :, g], v0[s])
+
+
+def test_block_permutation_gives_identical_bits(clean_status):
+    w = random_decode(12, 6, 40, 600, spare=20)
+    a = bits_of(run(w).out)
+    perm = np.random.default_rng(3).permutation(w.num_blocks).astype(np.int32)
+    w.block_tables = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1).astype(np.int32)
+    b = bits_of(run(w).out)
+    assert np.array_equal(a, b)
+
+
+def test_shared_prefix_blocks_give_identical_bits(clean_status):
+    shared = custom(13, prefix=[128, 200, 300], qlen=[1, 1, 1], shared_len=128, shared=(0, 1, 2))
+    private = custom(13, prefix=[128, 200, 300], qlen=[1, 1, 1])
+    private.q, private.k_all, private.v_all = shared.q, shared.k_all, shared.v_all
+    assert np.array_equal(bits_of(run(shared).out), bits_of(run(private).out))
+
+
+def test_nan_in_unused_slots_never_reaches_the_output(clean_status):
+    # contexts ending mid-block leave NaN-filled slots in their last block
+    w = random_decode(14, 8, 1, 64)
+    dw = run(w)
+    assert np.all(np.isfinite(dw.out_f64()))
+    assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype)
+
+
+def test_full_llama_decode_sampled(clean_status):
+    w = make_config("llama-decode")
+    dw = run(w)
+    got = dw.out_f64()
+    toks = np.random.default_rng(1).choice(w.num_tokens, 12, replace=False).astype(np.int32)
+    ref = oracle.workload_attention(w, tokens=toks)
+    assert_close(got[toks], ref, w.dtype, "llama-decode sample")
+    assert np.all(np.isfinite(got))
+
+
+def test_full_long_decode_sampled(clean_status):
+    w = make_config("long-decode")
+    dw = run(w)
+    got = dw.out_f64()
+    toks = np.array([0, 7, 15], dtype=np.int32)
+    ref = oracle.workload_attention(w, tokens=toks)
+    assert_close(got[toks], ref, w.dtype, "long-decode sample")
+    assert np.all(np.isfinite(got))
+
+
+def test_decode_is_deterministic(clean_status):
+    w = random_decode(15, 4, 200, 900)
+    dw = run(w, split=64)
+    a = bits_of(dw.out).copy()
+    dw.attention()
+    torch.cuda.synchronize()
+    assert np.array_equal(a, bits_of(dw.out))
