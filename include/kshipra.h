@@ -176,6 +176,37 @@ int kshipra_paged_attention(void* out, const void* q_rot, const void* k_arena, c
                             void* stream);
 
 /*
+ * Paged attention without any allocation and without a caller workspace.
+ * The paper has no counterpart; this is a convenience of this library.
+ *
+ * For callers that can't allocate device memory: a server that reserved all
+ * free device memory for its KV arena up front (a later cudaMalloc would
+ * fail), a host framework whose allocator owns every device byte, or a
+ * latency-critical loop that must not pay cudaMalloc's implicit
+ * synchronisation.  Same arguments, computation and errors as
+ * kshipra_paged_attention minus the workspace: the split-KV partials live in
+ * a fixed scratch array of KSHIPRA_NOALLOC_SCRATCH_BYTES bytes inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  Sizes whose partials need more than that are rejected with
+ * KSHIPRA_ERR_WORKSPACE_TOO_SMALL before anything is launched (query the need
+ * with kshipra_paged_attention_workspace_size).  The first call on a device
+ * looks up the scratch address on that device (make it before any stream
+ * capture).  All calls share the one array: calls that overlap on the GPU
+ * (different streams, or several host threads) race and corrupt each
+ * other's results; serialise them.  Nothing in the scratch has to start at
+ * zero: each call writes every partial it reads.
+ * Errors: as kshipra_paged_attention; KSHIPRA_ERR_CUDA also when the scratch
+ * address cannot be looked up.
+ */
+#define KSHIPRA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int kshipra_paged_attention_noalloc(void* out, const void* q_rot, const void* k_arena, const void* v_arena,
+                                    const int32_t* block_tables, const int32_t* context_lens,
+                                    const int32_t* query_start_loc, const int32_t* positions, int num_seqs,
+                                    int num_tokens, int max_query_len, int max_context_len, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                                    int num_blocks, float scale, int dtype, void* stream);
+
+/*
  * Reads the current device's status word into *code_out (host pointer) and
  * clears it, after waiting for `stream`.  0 means no kernel reported a
  * violation since the last read.  Errors: INVALID_ARG, CUDA.

@@ -122,6 +122,21 @@ def kshipra_paged_attention(out, q_rot, k_arena, v_arena, block_tables, context_
         float(scale), _dtype_code(q_rot), _ptr(workspace), ws_bytes, _stream(stream)), "kshipra_paged_attention")
 
 
+def kshipra_paged_attention_noalloc(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc,
+                                    positions, max_query_len: int, max_context_len: int, scale: float,
+                                    stream=None) -> None:
+    """kshipra_paged_attention without a workspace, for callers that can't
+    allocate device memory; uses the library's fixed scratch array (calls
+    that overlap on the GPU race)."""
+    num_tokens, num_q_heads, head_dim = q_rot.shape
+    num_blocks, num_kv_heads, block_size, _ = k_arena.shape
+    _check(_lib.load().kshipra_paged_attention_noalloc(
+        _ptr(out), _ptr(q_rot), _ptr(k_arena), _ptr(v_arena), _ptr(block_tables), _ptr(context_lens),
+        _ptr(query_start_loc), _ptr(positions), query_start_loc.shape[0] - 1, num_tokens, max_query_len,
+        max_context_len, num_q_heads, num_kv_heads, head_dim, block_size, block_tables.shape[1], num_blocks,
+        float(scale), _dtype_code(q_rot), _stream(stream)), "kshipra_paged_attention_noalloc")
+
+
 def kshipra_device_status(stream=None) -> int:
     code = ctypes.c_int32(0)
     _check(_lib.load().kshipra_device_status(ctypes.byref(code), _stream(stream)), "kshipra_device_status")
