@@ -1,0 +1,122 @@
+"""Chunked-prefill attention (tcgen05 kernel) and mixed batches on the GPU
+against the float64 oracle (pages "Building Kshipra" part 3, section 4:
+chunks at absolute positions after the cached prefix, causal mask over the
+chunk, online softmax over in-place arena blocks; section 5: mixed steps;
+section 3: shared prefix blocks)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, custom, random_decode
+from workloads import make_config
+from workloads.device import DeviceWorkload, bits_of
+
+pytestmark = pytest.mark.gpu
+
+
+def run(w, max_rows=None, split=None):
+    import paged_kv_cache_arena_gb300 as K
+    if max_rows is not None:
+        K.kshipra_set_option(K.KSHIPRA_OPT_DECODE_MAX_ROWS, max_rows)
+    if split is not None:
+        K.kshipra_set_option(K.KSHIPRA_OPT_SPLIT_TOKENS, split)
+    dw = DeviceWorkload(w)
+    dw.step()
+    torch.cuda.synchronize()
+    return dw
+
+
+CASES = {
+    # one 17-token chunk starting mid-block plus one decode (both kernels)
+    "tiny": lambda: make_config("tiny"),
+    # chunks spanning several key tiles, ragged query and key tiles
+    "g4-multi-tile": lambda: custom(21, prefix=[0, 130, 300], qlen=[200, 77, 129]),
+    "g1": lambda: custom(22, Hq=4, Hkv=4, prefix=[5, 250], qlen=[130, 40]),
+    "g2-d64": lambda: custom(23, Hq=8, Hkv=4, d=64, prefix=[17, 0], qlen=[100, 65]),
+    "g8": lambda: custom(24, Hq=16, Hkv=2, prefix=[33, 400], qlen=[20, 3]),
+    "g16-bs32": lambda: custom(25, Hq=32, Hkv=2, bs=32, prefix=[64, 7], qlen=[9, 30]),
+    "bf16-bs32": lambda: custom(26, bs=32, dtype="bf16", prefix=[100, 500], qlen=[90, 33]),
+    "d64-bf16": lambda: custom(27, Hq=16, Hkv=4, d=64, dtype="bf16", prefix=[129], qlen=[255]),
+    "shared-prefix": lambda: custom(28, Hq=8, Hkv=2, prefix=[64, 96, 200], qlen=[40, 1, 70], shared_len=64,
+                                    shared=(0, 1, 2)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_prefill_matches_oracle(clean_status, name):
+    w = CASES[name]()
+    dw = run(w)
+    assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype, name)
+
+
+@pytest.mark.parametrize("name", ["g4-multi-tile", "bf16-bs32", "tiny"])
+def test_everything_through_the_prefill_kernel(clean_status, name):
+    w = CASES[name]()
+    dw = run(w, max_rows=0)  # even single-token sequences on the tensor-core kernel
+    assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype, name)
+
+
+def test_decode_sequences_on_prefill_kernel(clean_status):
+    w = random_decode(29, 6, 1, 700)
+    dw = run(w, max_rows=0)
+    assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype)
+
+
+def test_decode_equals_last_row_of_prefill_across_kernels(clean_status):
+    chunk = custom(30, prefix=[100, 37], qlen=[60, 90])
+    full = run(chunk).out_f64()
+    dec = custom(30, prefix=[100, 37], qlen=[60, 90])
+    dec.prefix_lens = chunk.prefix_lens + chunk.query_lens - 1
+    dec.query_lens = np.ones_like(chunk.query_lens)
+    last = chunk.query_start_loc[1:] - 1
+    dec.q = chunk.q[last]
+    got = run(dec).out_f64()  # decode kernel
+    assert_close(got, full[last], "f16", "decode vs last prefill row")
+
+
+def test_prefill_block_permutation_gives_identical_bits(clean_status):
+    w = custom(31, prefix=[70, 300], qlen=[100, 64], spare=30)
+    a = bits_of(run(w).out)
+    perm = np.random.default_rng(4).permutation(w.num_blocks).astype(np.int32)
+    w.block_tables = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1).astype(np.int32)
+    assert np.array_equal(a, bits_of(run(w).out))
+
+
+def test_prefill_shared_prefix_gives_identical_bits(clean_status):
+    shared = custom(32, Hq=8, Hkv=2, prefix=[64, 80], qlen=[50, 70], shared_len=64, shared=(0, 1))
+    private = custom(32, Hq=8, Hkv=2, prefix=[64, 80], qlen=[50, 70])
+    private.q, private.k_all, private.v_all = shared.q, shared.k_all, shared.v_all
+    assert np.array_equal(bits_of(run(shared).out), bits_of(run(private).out))
+
+
+def test_first_chunk_token_sees_only_itself(clean_status):
+    w = custom(33, Hq=8, Hkv=2, prefix=[0], qlen=[70])
+    dw = run(w)
+    got = bits_of(dw.out)[0].reshape(2, 4, -1)
+    v0 = bits_of(dw.v_new)[0]
+    for g in range(4):
+        assert np.array_equal(got[:, g], v0)
+
+
+def test_full_chunked_prefill_sampled(clean_status):
+    w = make_config("chunked-prefill")
+    dw = run(w)
+    got = dw.out_f64()
+    assert np.all(np.isfinite(got))
+    rng = np.random.default_rng(2)
+    toks = np.sort(np.concatenate([rng.choice(w.num_tokens, 60, replace=False), [0, 511, 512, 2047]])).astype(np.int32)
+    assert_close(got[toks], oracle.workload_attention(w, tokens=toks), w.dtype, "chunked-prefill sample")
+
+
+def test_full_mixed_step_sampled(clean_status):
+    w = make_config("mixed")
+    dw = run(w)
+    got = dw.out_f64()
+    assert np.all(np.isfinite(got))
+    rng = np.random.default_rng(3)
+    chunk_tokens = rng.choice(int(w.query_start_loc[8]), 40, replace=False)
+    dec_tokens = rng.choice(np.arange(int(w.query_start_loc[8]), w.num_tokens), 40, replace=False)
+    toks = np.sort(np.concatenate([chunk_tokens, dec_tokens])).astype(np.int32)
+    assert_close(got[toks], oracle.workload_attention(w, tokens=toks), w.dtype, "mixed sample")
