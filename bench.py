@@ -190,14 +190,12 @@ def time_e2e(torch, dw, steps, stream):
 def gpu_launches_per_step(w, decode_max_rows=16):
     G = w.num_q_heads // w.num_kv_heads
     rows = w.query_lens * G
-    n = 1 + 1  # append, decode
-    import paged_kv_cache_arena_gb300 as K
-    ws = K.kshipra_paged_attention_workspace_size(w.num_seqs, w.num_tokens, w.max_context_len, w.num_q_heads,
-                                                  w.num_kv_heads, w.head_dim)
-    if ws > 0:
-        n += 1  # combine
+    n = 0
+    if (rows <= decode_max_rows).any():
+        n += 1  # decode (splits merged in the same kernel)
+    n += 1  # append
     if (rows > decode_max_rows).any():
-        n += 1  # prefill
+        n += 2  # prefill planning + persistent prefill
     return n
 
 
@@ -354,7 +352,7 @@ def gpu_arm(args, w):
                 "l2": "inputs larger than L2 (%.0f MB of KV per step)" % (kv / 1e6)},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk.get("hbm_gbs"),
                          "unit": "GB/s", "frac": round(achieved / pk.get("hbm_gbs"), 4), "traffic": None,
-                         "kernel": "paged attention call (decode_kernel + combine_kernel)",
+                         "kernel": "paged attention call (decode_kernel, split combine inside)",
                          "ms_per_launch": round(att_ms, 5), "peak_source": pk_src},
             "append_ms_per_step": round(statistics.mean(app), 5),
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

@@ -134,6 +134,7 @@ int check_heads(int num_q_heads, int num_kv_heads, int head_dim, int block_size,
   const int g = num_q_heads / num_kv_heads;
   if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16)
     return fail(KSHIPRA_ERR_UNSUPPORTED, "group size %d not in {1, 2, 4, 8, 16}", g);
+  if (num_kv_heads > 255) return fail(KSHIPRA_ERR_UNSUPPORTED, "num_kv_heads %d above 255", num_kv_heads);
   if (head_dim != 64 && head_dim != 128) return fail(KSHIPRA_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}", head_dim);
   if (block_size != 16 && block_size != 32)
     return fail(KSHIPRA_ERR_UNSUPPORTED, "block_size %d not in {16, 32}", block_size);
@@ -173,20 +174,27 @@ int split_tokens_for(int num_seqs, int max_context_len, int num_kv_heads, int sm
 struct WorkspacePlan {
   int split_tokens;
   int max_splits;
-  size_t o_bytes, ml_bytes, total;
+  int max_items;
+  size_t o_bytes, ml_bytes, counter_bytes, items_bytes, total;
 };
 
 WorkspacePlan plan_workspace(int num_seqs, int num_tokens, int max_context_len, int num_q_heads,
                              int num_kv_heads, int head_dim, int sm_count) {
   WorkspacePlan p{};
+  auto round256 = [](size_t x) { return (x + 255) / 256 * 256; };
   p.split_tokens = split_tokens_for(num_seqs, max_context_len, num_kv_heads, sm_count);
   p.max_splits = max_context_len > 0 ? (max_context_len + p.split_tokens - 1) / p.split_tokens : 1;
   if (p.max_splits < 1) p.max_splits = 1;
-  if (p.max_splits == 1 || g_opt_decode_max_rows.load() == 0) return p;  // no partials needed
-  const size_t rows = static_cast<size_t>(p.max_splits) * num_tokens * num_q_heads;
-  p.o_bytes = (rows * head_dim * sizeof(float) + 255) / 256 * 256;
-  p.ml_bytes = (rows * 2 * sizeof(float) + 255) / 256 * 256;
-  p.total = p.o_bytes + p.ml_bytes;
+  if (p.max_splits > 1 && g_opt_decode_max_rows.load() > 0) {  // decode partials and counters
+    const size_t rows = static_cast<size_t>(p.max_splits) * num_tokens * num_q_heads;
+    p.o_bytes = round256(rows * head_dim * sizeof(float));
+    p.ml_bytes = round256(rows * 2 * sizeof(float));
+    p.counter_bytes = round256(static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(unsigned));
+  }
+  // prefill work list + its length
+  p.max_items = num_tokens > 0 ? prefill_max_items(num_seqs, num_tokens, num_q_heads, num_kv_heads) : 0;
+  p.items_bytes = p.max_items > 0 ? round256(static_cast<size_t>(p.max_items) * sizeof(uint64_t) + sizeof(int)) : 0;
+  p.total = p.o_bytes + p.ml_bytes + p.counter_bytes + p.items_bytes;
   return p;
 }
 
@@ -327,6 +335,8 @@ int kshipra_paged_attention(void* out, const void* q_rot, const void* k_arena, c
   int rc = check_heads(num_q_heads, num_kv_heads, head_dim, block_size, dtype);
   if (rc) return rc;
   if ((rc = check_arena(num_blocks, num_kv_heads, block_size, max_blocks_per_seq))) return rc;
+  if (num_seqs >= (1 << 24) || max_query_len / (2 * (128 / (num_q_heads / num_kv_heads))) >= (1 << 16))
+    return fail(KSHIPRA_ERR_UNSUPPORTED, "num_seqs must stay below 2^24 and max_query_len below 2^16 tile pairs");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(KSHIPRA_ERR_INVALID_ARG, "scale must be positive");
   if (num_tokens == 0) return KSHIPRA_OK;
   if (max_context_len <= 0 || max_query_len <= 0)
@@ -353,8 +363,16 @@ int kshipra_paged_attention(void* out, const void* q_rot, const void* k_arena, c
   AttnArgs a{};
   a.out = out; a.q_rot = q_rot; a.block_tables = block_tables; a.context_lens = context_lens;
   a.query_start_loc = query_start_loc; a.positions = positions;
-  a.ws_o = plan.total ? static_cast<float*>(workspace) : nullptr;
-  a.ws_ml = plan.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.o_bytes) : nullptr;
+  char* ws = static_cast<char*>(workspace);
+  a.ws_o = plan.o_bytes ? reinterpret_cast<float*>(ws) : nullptr;
+  a.ws_ml = plan.ml_bytes ? reinterpret_cast<float*>(ws + plan.o_bytes) : nullptr;
+  a.ws_counters = plan.counter_bytes ? reinterpret_cast<unsigned*>(ws + plan.o_bytes + plan.ml_bytes) : nullptr;
+  const size_t items_off = plan.o_bytes + plan.ml_bytes + plan.counter_bytes;
+  a.ws_items = plan.items_bytes ? reinterpret_cast<uint64_t*>(ws + items_off) : nullptr;
+  a.ws_item_count =
+      plan.items_bytes ? reinterpret_cast<int*>(ws + items_off + static_cast<size_t>(plan.max_items) * 8) : nullptr;
+  a.max_items = plan.max_items;
+  a.sm_count = sms;
   a.num_seqs = num_seqs; a.num_tokens = num_tokens; a.max_query_len = max_query_len;
   a.max_context_len = max_context_len; a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
   a.group = num_q_heads / num_kv_heads; a.head_dim = head_dim; a.block_size = block_size;
@@ -370,8 +388,10 @@ int kshipra_paged_attention(void* out, const void* q_rot, const void* k_arena, c
   if ((rc = arena_map(&kmap, k_arena, dtype, head_dim, rows, 16))) return rc;
   if ((rc = arena_map(&vmap, v_arena, dtype, head_dim, rows, 16))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a.ws_counters &&
+      (e = cudaMemsetAsync(a.ws_counters, 0, plan.counter_bytes, s)) != cudaSuccess)
+    return cuda_fail(e, "clearing split counters");
   if ((e = launch_decode(a, kmap, vmap, s)) != cudaSuccess) return cuda_fail(e, "decode kernel launch");
-  if ((e = launch_combine(a, s)) != cudaSuccess) return cuda_fail(e, "combine kernel launch");
   // prefill class: any sequence with more rows than the decode kernel takes
   if (static_cast<long long>(max_query_len) * a.group > a.decode_max_rows) {
     CUtensorMap kmap_p, vmap_p;

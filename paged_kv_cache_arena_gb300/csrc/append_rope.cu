@@ -7,7 +7,7 @@
 // and section 4 (RoPE at absolute positions: a chunk after P cached tokens
 // starts at position P).
 //
-// One CTA per token.  The rotation is done in float64 from the caller's
+// One warp per (token, head).  The rotation is done in float64 from the caller's
 // (cos, sin) table with separate products and one add, then rounded once to
 // the storage type, so the arena image is reproducible bit for bit.  The
 // volume is small (num_tokens x (Hq + Hkv) x head_dim elements per call); the
@@ -18,7 +18,8 @@
 namespace kshipra {
 namespace {
 
-constexpr int kAppendThreads = 128;
+constexpr int kAppendWarps = 4;
+constexpr int kAppendThreads = 32 * kAppendWarps;
 
 // Rotates pairs (i, i + d/2) and (i + 1, i + 1 + d/2) of one head row.
 template <bool kBf16>
@@ -44,10 +45,16 @@ __device__ __forceinline__ void rotate_two_pairs(const uint16_t* src, uint16_t* 
   *reinterpret_cast<uint32_t*>(dst + i + half) = ohi;
 }
 
+// One warp per (token, head): warps of blockIdx.y cover q heads first, then
+// kv heads (k rotated into the arena, v copied).  Lane i rotates pairs 2i and
+// 2i + 1; with head_dim 64 the upper half of the warp idles.
 template <bool kBf16>
 __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendArgs a) {
   const int t = blockIdx.x;
-  if (t >= a.num_tokens) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nq = a.q != nullptr ? a.num_q_heads : 0;
+  const int hh = blockIdx.y * kAppendWarps + warp;  // head slot: [0, nq) q heads, then kv heads
+  if (t >= a.num_tokens || hh >= nq + a.num_kv_heads) return;
   // sequence of token t: the last s with query_start_loc[s] <= t
   int lo = 0, hi = a.num_seqs - 1;
   while (lo < hi) {
@@ -56,57 +63,48 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendArgs 
     else hi = mid - 1;
   }
   const int s = lo;
-  const int pos = __ldg(a.positions + t);
+  const bool first = blockIdx.y == 0 && threadIdx.x == 0;  // reports once per token
   if (t < __ldg(a.query_start_loc + s) || t >= __ldg(a.query_start_loc + s + 1)) {  // outside every sequence
-    if (threadIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
+    if (first) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
     return;
   }
+  const int pos = __ldg(a.positions + t);
   if (pos < 0 || pos >= a.rope_max_pos || pos / a.block_size >= a.max_blocks_per_seq) {
-    if (threadIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_POSITION);
+    if (first) report(a.status, KSHIPRA_DEV_BAD_POSITION);
     return;
   }
-  const int blk = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + pos / a.block_size);
-  const bool blk_ok = blk >= 0 && blk < a.num_blocks;
-  if (!blk_ok && threadIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
-  const int slot = pos % a.block_size;
-  const int D = a.head_dim, half = D / 2, pairs2 = half / 2;  // two pairs per work item
+  const int D = a.head_dim, half = D / 2;
   const double* cs = a.rope_table + static_cast<size_t>(pos) * D;  // [d/2][2] for this position
-
-  // q rows (optional)
-  if (a.q != nullptr) {
-    const uint16_t* qsrc = static_cast<const uint16_t*>(a.q) + static_cast<size_t>(t) * a.num_q_heads * D;
-    uint16_t* qdst = static_cast<uint16_t*>(a.q_rot) + static_cast<size_t>(t) * a.num_q_heads * D;
-    for (int w = threadIdx.x; w < a.num_q_heads * pairs2; w += blockDim.x) {
-      const int h = w / pairs2, i = 2 * (w % pairs2);
-      rotate_two_pairs<kBf16>(qsrc + h * D, qdst + h * D, i, half, cs);
-    }
+  const int i = 2 * lane;                                           // first pair of this lane
+  if (hh < nq) {
+    const size_t row = (static_cast<size_t>(t) * a.num_q_heads + hh) * D;
+    if (i < half)
+      rotate_two_pairs<kBf16>(static_cast<const uint16_t*>(a.q) + row, static_cast<uint16_t*>(a.q_rot) + row, i,
+                              half, cs);
+    return;
   }
-  if (!blk_ok) return;
-  // k rows -> arena, rotated
-  const uint16_t* ksrc = static_cast<const uint16_t*>(a.k) + static_cast<size_t>(t) * a.num_kv_heads * D;
-  uint16_t* karena = static_cast<uint16_t*>(a.k_arena);
-  for (int w = threadIdx.x; w < a.num_kv_heads * pairs2; w += blockDim.x) {
-    const int h = w / pairs2, i = 2 * (w % pairs2);
-    const size_t row = (static_cast<size_t>(blk) * a.num_kv_heads + h) * a.block_size + slot;
-    rotate_two_pairs<kBf16>(ksrc + h * D, karena + row * D, i, half, cs);
+  const int h = hh - nq;
+  const int blk = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + pos / a.block_size);
+  if (blk < 0 || blk >= a.num_blocks) {
+    if (lane == 0) report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
+    return;
   }
-  // v rows -> arena, bit copy in 16-byte pieces
-  const uint4* vsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) +
-                                                     static_cast<size_t>(t) * a.num_kv_heads * D);
-  uint16_t* varena = static_cast<uint16_t*>(a.v_arena);
-  const int vec_per_row = D / 8;
-  for (int w = threadIdx.x; w < a.num_kv_heads * vec_per_row; w += blockDim.x) {
-    const int h = w / vec_per_row, c = w % vec_per_row;
-    const size_t row = (static_cast<size_t>(blk) * a.num_kv_heads + h) * a.block_size + slot;
-    reinterpret_cast<uint4*>(varena + row * D)[c] = vsrc[w];
-  }
+  const size_t src = (static_cast<size_t>(t) * a.num_kv_heads + h) * D;
+  const size_t dst = ((static_cast<size_t>(blk) * a.num_kv_heads + h) * a.block_size + pos % a.block_size) * D;
+  if (i < half)
+    rotate_two_pairs<kBf16>(static_cast<const uint16_t*>(a.k) + src, static_cast<uint16_t*>(a.k_arena) + dst, i,
+                            half, cs);
+  if (lane < D / 8)  // value row: bit copy in 16-byte pieces
+    reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.v_arena) + dst)[lane] =
+        reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) + src)[lane];
 }
 
 }  // namespace
 
 cudaError_t launch_append_rope(const AppendArgs& a, cudaStream_t stream) {
   if (a.num_tokens == 0) return cudaSuccess;
-  dim3 grid(a.num_tokens), block(kAppendThreads);
+  const int heads = (a.q != nullptr ? a.num_q_heads : 0) + a.num_kv_heads;
+  dim3 grid(a.num_tokens, (heads + kAppendWarps - 1) / kAppendWarps), block(kAppendThreads);
   if (a.dtype == KSHIPRA_DTYPE_BF16)
     append_rope_kernel<true><<<grid, block, 0, stream>>>(a);
   else

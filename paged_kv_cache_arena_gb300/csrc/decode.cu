@@ -1,4 +1,4 @@
-// Split-KV decode attention over the block arena, and the split-combine pass.
+// Split-KV decode attention over the block arena, with the split combine.
 //
 // Pages "Building Kshipra" part 3 (kshipra-3), section 4: attention runs an
 // online softmax (running max m, running sum l, rescaled accumulator o) over
@@ -25,7 +25,8 @@
 //    zeroed value rows.
 //  - Warps merge through shared memory; a single-split sequence writes its
 //    rounded output directly, otherwise the partial (m, l, o) goes to the
-//    workspace and combine_kernel merges the splits.
+//    workspace, and the CTA that finishes last for its (sequence, kv head)
+//    (atomic ticket) merges all splits.
 #include <float.h>
 
 #include "common.cuh"
@@ -281,6 +282,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* kmap, const CUten
   __syncthreads();
   if (any_fail) return;
 
+  const size_t split_stride = static_cast<size_t>(a.num_tokens) * a.num_q_heads;
   for (int idx = threadIdx.x; idx < nrows * D; idx += kThreads) {
     const int r = idx / D, d = idx % D;
     float M = kNegInf;
@@ -301,13 +303,41 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* kmap, const CUten
     if (nsplit == 1) {
       static_cast<uint16_t*>(a.out)[orow * D + d] = round_f32<kBf16>(O / Lsum);
     } else {
-      const size_t prow = static_cast<size_t>(split) * a.num_tokens * a.num_q_heads + orow;
+      const size_t prow = static_cast<size_t>(split) * split_stride + orow;
       a.ws_o[prow * D + d] = O;
       if (d == 0) {
         a.ws_ml[prow * 2] = M;
         a.ws_ml[prow * 2 + 1] = Lsum;
       }
     }
+  }
+  if (nsplit == 1) return;
+
+  // Split combine, done by whichever CTA of this (sequence, kv head) finishes
+  // last: M = max_i m_i, L = sum_i l_i 2^{(m_i - M) c}, out = sum_i o_i 2^{(m_i - M) c} / L.
+  __shared__ unsigned is_last;
+  __threadfence();  // this CTA's partials are visible before its ticket
+  __syncthreads();
+  if (threadIdx.x == 0)
+    is_last = atomicAdd(a.ws_counters + static_cast<size_t>(s) * a.num_kv_heads + h, 1u) ==
+              static_cast<unsigned>(nsplit - 1);
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  for (int idx = threadIdx.x; idx < nrows * D; idx += kThreads) {
+    const int r = idx / D, d = idx % D;
+    const size_t orow = static_cast<size_t>(q0 + r / G) * a.num_q_heads + h * G + r % G;
+    float M = kNegInf;
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(a.ws_ml + (sp * split_stride + orow) * 2));
+    float Lsum = 0.f, O = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const size_t prow = sp * split_stride + orow;
+      const float mi = __ldcg(a.ws_ml + prow * 2);
+      const float f = mi == kNegInf ? 0.f : ex2((mi - M) * c2);
+      Lsum = fmaf(__ldcg(a.ws_ml + prow * 2 + 1), f, Lsum);
+      O = fmaf(__ldcg(a.ws_o + prow * D + d), f, O);
+    }
+    static_cast<uint16_t*>(a.out)[orow * D + d] = round_f32<kBf16>(O / Lsum);
   }
 }
 
@@ -339,38 +369,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     decode_body<D, kBf16, 2>(&kmap, &vmap, a, smem, s, h, split, q0, nrows, ctx, nsplit);
 }
 
-// Merges the per-split partials of multi-split decode sequences:
-//   M = max_i m_i,  L = sum_i l_i 2^{(m_i - M) c},  out = sum_i o_i 2^{(m_i - M) c} / L.
-template <int D, bool kBf16>
-__global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
-  const int h = blockIdx.x, s = blockIdx.y;
-  const int q0 = __ldg(a.query_start_loc + s);
-  const int qlen = __ldg(a.query_start_loc + s + 1) - q0;
-  const int nrows = qlen * a.group;
-  if (q0 < 0 || q0 + qlen > a.num_tokens || qlen <= 0 || nrows > a.decode_max_rows) return;
-  const int ctx = __ldg(a.context_lens + s);
-  const int nsplit = ceil_div(ctx, a.split_tokens);
-  if (nsplit <= 1 || nsplit > a.max_splits || ctx > a.max_blocks_per_seq * a.block_size) return;
-  const float c2 = a.scale_log2;
-  const size_t split_stride = static_cast<size_t>(a.num_tokens) * a.num_q_heads;
-  for (int idx = threadIdx.x; idx < nrows * D; idx += blockDim.x) {
-    const int r = idx / D, d = idx % D;
-    const int tok = q0 + r / a.group, head = h * a.group + r % a.group;
-    const size_t orow = static_cast<size_t>(tok) * a.num_q_heads + head;
-    float M = kNegInf;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, a.ws_ml[(sp * split_stride + orow) * 2]);
-    float Lsum = 0.f, O = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const size_t prow = sp * split_stride + orow;
-      const float mi = a.ws_ml[prow * 2];
-      const float f = mi == kNegInf ? 0.f : ex2((mi - M) * c2);
-      Lsum = fmaf(a.ws_ml[prow * 2 + 1], f, Lsum);
-      O = fmaf(a.ws_o[prow * D + d], f, O);
-    }
-    static_cast<uint16_t*>(a.out)[orow * D + d] = round_f32<kBf16>(O / Lsum);
-  }
-}
-
 template <int D, bool kBf16>
 cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t stream) {
@@ -392,20 +390,6 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
   if (a.head_dim == 128)
     return bf ? launch_decode_t<128, true>(a, kmap, vmap, stream) : launch_decode_t<128, false>(a, kmap, vmap, stream);
   return bf ? launch_decode_t<64, true>(a, kmap, vmap, stream) : launch_decode_t<64, false>(a, kmap, vmap, stream);
-}
-
-cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream) {
-  if (a.num_seqs == 0 || a.decode_max_rows == 0 || a.max_splits <= 1) return cudaSuccess;
-  dim3 grid(a.num_kv_heads, a.num_seqs);
-  const bool bf = a.dtype == KSHIPRA_DTYPE_BF16;
-  if (a.head_dim == 128) {
-    if (bf) combine_kernel<128, true><<<grid, 128, 0, stream>>>(a);
-    else combine_kernel<128, false><<<grid, 128, 0, stream>>>(a);
-  } else {
-    if (bf) combine_kernel<64, true><<<grid, 128, 0, stream>>>(a);
-    else combine_kernel<64, false><<<grid, 128, 0, stream>>>(a);
-  }
-  return cudaGetLastError();
 }
 
 }  // namespace kshipra

@@ -42,6 +42,11 @@ struct AttnArgs {
   const int32_t* positions;
   float* ws_o;   // [max_splits][num_tokens][num_q_heads][head_dim] partial accumulators
   float* ws_ml;  // [max_splits][num_tokens][num_q_heads][2] partial (max, sum)
+  unsigned* ws_counters;  // [num_seqs][num_kv_heads] finished splits, zeroed by the host each call
+  uint64_t* ws_items;     // prefill work list (written by the planning kernel)
+  int* ws_item_count;
+  int max_items;          // capacity of ws_items
+  int sm_count;           // CTAs of the persistent prefill kernel
   unsigned* status;
   int num_seqs, num_tokens, max_query_len, max_context_len;
   int num_q_heads, num_kv_heads, group, head_dim, block_size, max_blocks_per_seq, num_blocks;
@@ -51,12 +56,17 @@ struct AttnArgs {
   int dtype;
 };
 
-// Split-KV decode (mma.sync on staged TMA tiles) followed by the combine pass.
+// Split-KV decode (mma.sync on staged TMA tiles); the last split of each
+// (sequence, kv head) to finish merges all partials.
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
-cudaError_t launch_combine(const AttnArgs& a, cudaStream_t stream);
 
-// Chunked prefill on tcgen05 / TMEM.
+// Upper bound on the prefill work items of a call (pairs of 128-row query
+// tiles per (sequence, kv head)).
+int prefill_max_items(int num_seqs, int num_tokens, int num_q_heads, int num_kv_heads);
+
+// Chunked prefill on tcgen05 / TMEM: planning kernel, then the persistent
+// attention kernel.
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            const CUtensorMap& qmap, cudaStream_t stream);
 

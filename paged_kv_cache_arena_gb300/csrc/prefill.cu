@@ -7,27 +7,36 @@
 // place from the arena.  Section 1: keys of position p live in slot
 // p % block_size of physical block block_tables[s][p / block_size].
 //
-// Work unit (one CTA): 128 query rows = 128/G consecutive tokens x the G
-// query heads of one kv head (GQA packing: every K/V tile is loaded once for
-// all G heads), against 128-key tiles of that sequence.  Key tiles that lie
-// entirely past the tile's last position are never visited; only tiles that
-// cross a row's position are masked element by element.
+// Query tiles: 128 rows = 128/G consecutive tokens x the G query heads of one
+// kv head (GQA packing: every K/V tile serves all G heads).  A work item is a
+// pair of adjacent query tiles (A, B) of one (sequence, kv head); both walk
+// the same 128-key tiles, keys 0 .. (last position of the pair), so each K/V
+// tile is fetched once for 256 query rows.  Key tiles past the pair's last
+// position are never visited; tiles that cross a row's position are masked
+// element by element.
 //
-// Roles (192 threads):
-//  - warp 4 (one lane): TMA producer.  The Q tile is one 3-D box per 64-column
-//    half; each K/V tile is 128 / block_size boxes of one arena block each,
+// A small planning kernel lists the items with their cost (key tiles) and
+// sorts them, heaviest first; the persistent attention kernel (one CTA per
+// SM) walks that list in snake order.
+//
+// Roles in the attention kernel (320 threads):
+//  - warp 8 (one lane): TMA producer.  Q_A and Q_B are 3-D boxes (token x head
+//    x 64 columns); each K/V tile is 128 / block_size arena-block boxes
 //    addressed through the block table, double-buffered.
-//  - warp 5 (one lane): tcgen05.mma issuer.  S = Q K^T (M 128, N 128, K d)
-//    into TMEM columns [0, 128); O += P V (M 128, N d, K 128) into TMEM
-//    columns [128, 128 + d), V read MN-major straight from its arena layout.
-//    Completion is signalled with tcgen05.commit on mbarriers.
-//  - warps 0-3: softmax.  Thread r owns row r (TMEM lane r): loads its S row,
-//    applies the causal mask, updates the running max / sum, writes the
-//    probabilities as fp16/bf16 into shared memory (K-major, 128-byte
-//    swizzle) for the PV MMA, rescales its O row in TMEM when the max grows,
-//    and finally normalises and stores the output row.
-// Every wait is bounded (see mbar_wait); on a timeout all roles stop, drain
-// their outstanding copies / MMAs and release tensor memory.
+//  - warp 9 (one lane): tcgen05.mma issuer, ping-pong between the tiles:
+//    S_X = Q_X K^T (M 128, N 128, K d) into TMEM, then O_X += P_X V (M 128,
+//    N d, K 128) with P_X read from TMEM (written over S_X by the softmax) and
+//    V read MN-major in its arena layout.  While one tile's softmax runs, the
+//    tensor core works on the other tile.
+//  - warps 0-3 / 4-7: softmax of tile A / B.  Thread r owns row r (TMEM lane
+//    r): loads its S row, masks, keeps the running max / sum (the reference
+//    max is only raised when the row max passes it by 2^8, so O is rarely
+//    rescaled), writes P as fp16/bf16 back into TMEM, and at the end of the
+//    item normalises O and stores the output row.
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+d), O_B [384,384+d);
+// P_X occupies the first 64 columns of S_X.
+// Every wait is bounded (mbar_wait); on a timeout all roles stop, drain their
+// outstanding copies / MMAs and release tensor memory.
 #include <float.h>
 
 #include "common.cuh"
@@ -36,41 +45,44 @@
 namespace kshipra {
 namespace {
 
-constexpr int kTile = 128;  // query rows per CTA and keys per tile
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kTile = 128;  // query rows per tile and keys per key tile
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kStages = 2;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
 constexpr float kNegInf = -INFINITY;
+constexpr int kPlanThreads = 1024;
+constexpr int kSortCapacity = 4096;  // items sorted in shared memory; longer lists keep plan order
 
 template <int D>
 struct PrefillLayout {
   static constexpr int kRegions = D / 64;
   static constexpr int kRegionBytes = kTile * 128;  // 128 rows x 128 B
   static constexpr int kTileBytes = kRegions * kRegionBytes;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kQA = 0;
+  static constexpr int kQB = kQA + kTileBytes;
+  static constexpr int kK = kQB + kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kP = kV + kStages * kTileBytes;
-  static constexpr int kBar = kP + 2 * kRegionBytes;  // P: 128 rows x 128 keys
-  // barriers: q, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full, s_free,
-  // p_full, o_done, drain; then the TMEM base address
-  static constexpr int kNumBars = 14;
+  static constexpr int kBar = kV + kStages * kTileBytes;
+  // q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
+  // p_full[2], o_full[2], o_free[2], drain; then the TMEM base address
+  static constexpr int kNumBars = 19;
   static constexpr int kBytes = kBar + kNumBars * 8 + 16;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
 struct Bars {
-  uint64_t* q;
-  uint64_t* k_full;
-  uint64_t* k_empty;
-  uint64_t* v_full;
-  uint64_t* v_empty;
-  uint64_t* s_full;
-  uint64_t* s_free;
-  uint64_t* p_full;
-  uint64_t* o_done;
+  uint64_t* q_full;
+  uint64_t* q_empty;
+  uint64_t* k_full;   // [2]
+  uint64_t* k_empty;  // [2]
+  uint64_t* v_full;   // [2]
+  uint64_t* v_empty;  // [2]
+  uint64_t* s_full;   // [2] per query tile
+  uint64_t* p_full;   // [2]
+  uint64_t* o_full;   // [2]
+  uint64_t* o_free;   // [2]
   uint64_t* drain;
 };
 
@@ -83,8 +95,134 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+// A wait whose outcome is the same for all 32 lanes, so that warp-collective
+// instructions after it never run with lanes missing.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
+// ---------------------------------------------------------------- work items
+//
+// item = cost (16 bits) | sequence (24) | tile pair (16) | kv head (8); sorting
+// the 64-bit values in descending order puts the most expensive items first.
+
+__host__ __device__ constexpr uint64_t item_pack(uint32_t cost, uint32_t s, uint32_t pair, uint32_t h) {
+  return (static_cast<uint64_t>(cost) << 48) | (static_cast<uint64_t>(s) << 24) |
+         (static_cast<uint64_t>(pair) << 8) | h;
+}
+
+struct Item {
+  int s, pair, h;
+};
+
+__device__ __forceinline__ Item item_unpack(uint64_t v) {
+  return Item{static_cast<int>((v >> 24) & 0xFFFFFF), static_cast<int>((v >> 8) & 0xFFFF),
+              static_cast<int>(v & 0xFF)};
+}
+
+// Index of this CTA's r-th item (snake order over the sorted list).
+__device__ __forceinline__ int item_index(int r) {
+  return r * gridDim.x + ((r & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
+}
+
+struct PairGeom {
+  int q0;        // first token of the sequence
+  int tok_a;     // first token (sequence-relative) of tile A
+  int n_a, n_b;  // valid tokens in tiles A and B (n_b may be 0)
+  int nkeys;     // keys 0..nkeys-1 cover every row of the pair
+  int ntiles;    // 128-key tiles (0 when the item's lengths are inconsistent)
+};
+
+template <int G>
+__device__ __forceinline__ PairGeom pair_geom(const AttnArgs& a, int s, int pair) {
+  constexpr int TQ = kTile / G;
+  PairGeom p{};
+  p.q0 = __ldg(a.query_start_loc + s);
+  const int qlen = __ldg(a.query_start_loc + s + 1) - p.q0;
+  p.tok_a = 2 * pair * TQ;
+  p.n_a = min(TQ, qlen - p.tok_a);
+  p.n_b = max(0, min(TQ, qlen - p.tok_a - TQ));
+  const int ctx = __ldg(a.context_lens + s);
+  const bool shape_ok = p.q0 >= 0 && p.q0 + qlen <= a.num_tokens && p.n_a > 0;
+  const int pos_first = shape_ok ? __ldg(a.positions + p.q0 + p.tok_a) : -1;
+  const int pos_last = shape_ok ? __ldg(a.positions + p.q0 + p.tok_a + p.n_a + p.n_b - 1) : -1;
+  const bool ok = shape_ok && ctx > 0 && ctx <= a.max_blocks_per_seq * a.block_size && pos_first >= 0 &&
+                  pos_first <= pos_last && pos_last < ctx;
+  p.nkeys = ok ? pos_last + 1 : 0;
+  p.ntiles = ceil_div(p.nkeys, kTile);
+  return p;
+}
+
+// Lists the prefill items (sequences with query_len x group rows above the
+// decode threshold), sorts them by cost and writes them to items[]; *count
+// receives their number.  One CTA.
+template <int G>
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const AttnArgs a, uint64_t* items,
+                                                                     int* count, int max_items) {
+  constexpr int TQ = kTile / G;
+  __shared__ uint64_t buf[kSortCapacity];
+  __shared__ int scan[kPlanThreads];
+  __shared__ int base;
+  if (threadIdx.x == 0) base = 0;
+  __syncthreads();
+  for (int s0 = 0; s0 < a.num_seqs; s0 += kPlanThreads) {
+    const int s = s0 + threadIdx.x;
+    int pairs = 0, q0 = 0, qlen = 0;
+    if (s < a.num_seqs) {
+      q0 = __ldg(a.query_start_loc + s);
+      qlen = __ldg(a.query_start_loc + s + 1) - q0;
+      if (q0 >= 0 && qlen > 0 && q0 + qlen <= a.num_tokens && qlen * G > a.decode_max_rows)
+        pairs = ceil_div(ceil_div(qlen, TQ), 2);
+    }
+    const int n = pairs * a.num_kv_heads;
+    scan[threadIdx.x] = n;
+    __syncthreads();
+    for (int off = 1; off < kPlanThreads; off <<= 1) {  // inclusive scan
+      const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
+      __syncthreads();
+      scan[threadIdx.x] += v;
+      __syncthreads();
+    }
+    int out = base + scan[threadIdx.x] - n;
+    for (int p = 0; p < pairs; ++p) {
+      const int last = min(qlen, (2 * p + 2) * TQ) - 1;
+      const int nkeys = __ldg(a.positions + q0 + last) + 1;
+      const uint32_t cost = static_cast<uint32_t>(min(max(ceil_div(nkeys, kTile), 0), 0xFFFF));
+      for (int h = 0; h < a.num_kv_heads; ++h, ++out) {
+        if (out >= max_items) continue;
+        const uint64_t v = item_pack(cost, s, p, h);
+        if (out < kSortCapacity) buf[out] = v;
+        items[out] = v;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == kPlanThreads - 1) base += scan[threadIdx.x];
+    __syncthreads();
+  }
+  const int total = min(base, max_items);
+  if (total <= kSortCapacity) {  // bitonic sort, descending, padded with zeros
+    int n2 = 1;
+    while (n2 < total) n2 <<= 1;
+    for (int i = total + threadIdx.x; i < n2; i += kPlanThreads) buf[i] = 0;
+    __syncthreads();
+    for (int k = 2; k <= n2; k <<= 1)
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = threadIdx.x; i < n2; i += kPlanThreads) {
+          const int l = i ^ j;
+          if (l > i) {
+            const uint64_t x = buf[i], y = buf[l];
+            const bool desc = (i & k) == 0;
+            if (desc ? x < y : x > y) {
+              buf[i] = y;
+              buf[l] = x;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    for (int i = threadIdx.x; i < total; i += kPlanThreads) items[i] = buf[i];
+  }
+  if (threadIdx.x == 0) *count = total;
 }
 
 // ---------------------------------------------------------------- producer
@@ -92,55 +230,71 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 template <int D, int G>
 __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUtensorMap* vmap,
                                               const CUtensorMap* qmap, const AttnArgs& a, uint8_t* smem,
-                                              const Bars& b, int s, int h, int tok0, int nkeys, int ntiles) {
+                                              const Bars& b, const uint64_t* items, int count) {
   using L = PrefillLayout<D>;
+  constexpr int TQ = kTile / G;
   prefetch_tensormap(qmap);
   prefetch_tensormap(kmap);
   prefetch_tensormap(vmap);
-  mbar_arrive_expect_tx(b.q, L::kTileBytes);  // out-of-range tokens are zero-filled, bytes still count
-#pragma unroll
-  for (int r = 0; r < L::kRegions; ++r) tma_load_3d(smem + L::kQ + r * L::kRegionBytes, qmap, 64 * r, h * G, tok0, b.q);
-
   const int bs = a.block_size;
   const int blocks_per_tile = kTile / bs;
-  const int oob_row = a.num_blocks * a.num_kv_heads * bs;
-  const int32_t* table = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
+  const int oob_row = a.num_blocks * a.num_kv_heads * bs;  // past the tensor: zero fill
+  int g = 0;                                               // key tiles issued by this CTA
+  int items_done = 0;
   int issued_k[kStages] = {0, 0}, issued_v[kStages] = {0, 0};
   bool ok = true;
-  for (int j = 0; j < ntiles && ok; ++j) {
-    const int st = j & 1, use = j >> 1;
-    const int kend = min(kTile * (j + 1), nkeys);
-    const int nb = ceil_div(kend - kTile * j, bs);
-    const uint32_t bytes = static_cast<uint32_t>(nb * bs * 128 * L::kRegions);
-    int rows[kTile / 16];
-    for (int i = 0; i < nb; ++i) {
-      const int blk = __ldg(table + j * blocks_per_tile + i);
-      if (blk < 0 || blk >= a.num_blocks) {
-        report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
-        rows[i] = oob_row;
-      } else {
-        rows[i] = (blk * a.num_kv_heads + h) * bs;
-      }
+  for (int r = 0; ok; ++r) {
+    const int idx = item_index(r);
+    if (idx >= count) break;
+    const Item it = item_unpack(items[idx]);
+    const PairGeom p = pair_geom<G>(a, it.s, it.pair);
+    if (p.ntiles == 0) {
+      report(a.status, KSHIPRA_DEV_BAD_POSITION);
+      continue;
     }
-    if (j >= kStages && !mbar_wait(&b.k_empty[st], (use - 1) & 1, a.status)) { ok = false; break; }
-    mbar_arrive_expect_tx(&b.k_full[st], bytes);
-    uint8_t* kdst = smem + L::kK + st * L::kTileBytes;
-    for (int i = 0; i < nb; ++i)
+    if (items_done > 0 && !mbar_wait(b.q_empty, (items_done - 1) & 1, a.status)) { ok = false; break; }
+    mbar_arrive_expect_tx(b.q_full, 2 * L::kTileBytes);  // zero-filled rows still count
 #pragma unroll
-      for (int r = 0; r < L::kRegions; ++r)
-        tma_load_2d(kdst + r * L::kRegionBytes + i * bs * 128, kmap, 64 * r, rows[i], &b.k_full[st]);
-    issued_k[st] = j + 1;
-    if (j >= kStages && !mbar_wait(&b.v_empty[st], (use - 1) & 1, a.status)) { ok = false; break; }
-    mbar_arrive_expect_tx(&b.v_full[st], bytes);
-    uint8_t* vdst = smem + L::kV + st * L::kTileBytes;
-    for (int i = 0; i < nb; ++i)
+    for (int reg = 0; reg < L::kRegions; ++reg) {
+      tma_load_3d(smem + L::kQA + reg * L::kRegionBytes, qmap, 64 * reg, it.h * G, p.q0 + p.tok_a, b.q_full);
+      tma_load_3d(smem + L::kQB + reg * L::kRegionBytes, qmap, 64 * reg, it.h * G, p.q0 + p.tok_a + TQ, b.q_full);
+    }
+    ++items_done;
+    const int32_t* table = a.block_tables + static_cast<size_t>(it.s) * a.max_blocks_per_seq;
+    for (int j = 0; j < p.ntiles; ++j, ++g) {
+      const int st = g & 1, use = g >> 1;
+      const int nb = ceil_div(min(kTile * (j + 1), p.nkeys) - kTile * j, bs);
+      const uint32_t bytes = static_cast<uint32_t>(nb * bs * 128 * L::kRegions);
+      int rows[kTile / 16];
+      for (int i = 0; i < nb; ++i) {
+        const int blk = __ldg(table + j * blocks_per_tile + i);
+        if (blk < 0 || blk >= a.num_blocks) {
+          report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
+          rows[i] = oob_row;
+        } else {
+          rows[i] = (blk * a.num_kv_heads + it.h) * bs;
+        }
+      }
+      if (g >= kStages && !mbar_wait(&b.k_empty[st], (use - 1) & 1, a.status)) { ok = false; break; }
+      mbar_arrive_expect_tx(&b.k_full[st], bytes);
+      uint8_t* kdst = smem + L::kK + st * L::kTileBytes;
+      for (int i = 0; i < nb; ++i)
 #pragma unroll
-      for (int r = 0; r < L::kRegions; ++r)
-        tma_load_2d(vdst + r * L::kRegionBytes + i * bs * 128, vmap, 64 * r, rows[i], &b.v_full[st]);
-    issued_v[st] = j + 1;
+        for (int reg = 0; reg < L::kRegions; ++reg)
+          tma_load_2d(kdst + reg * L::kRegionBytes + i * bs * 128, kmap, 64 * reg, rows[i], &b.k_full[st]);
+      issued_k[st] = g + 1;
+      if (g >= kStages && !mbar_wait(&b.v_empty[st], (use - 1) & 1, a.status)) { ok = false; break; }
+      mbar_arrive_expect_tx(&b.v_full[st], bytes);
+      uint8_t* vdst = smem + L::kV + st * L::kTileBytes;
+      for (int i = 0; i < nb; ++i)
+#pragma unroll
+        for (int reg = 0; reg < L::kRegions; ++reg)
+          tma_load_2d(vdst + reg * L::kRegionBytes + i * bs * 128, vmap, 64 * reg, rows[i], &b.v_full[st]);
+      issued_v[st] = g + 1;
+    }
   }
   if (!ok) {  // let every copy this thread started land before the CTA moves on
-    drain_wait(b.q, 0);
+    if (items_done) drain_wait(b.q_full, (items_done - 1) & 1);
     for (int st = 0; st < kStages; ++st) {
       if (issued_k[st]) drain_wait(&b.k_full[st], ((issued_k[st] - 1) >> 1) & 1);
       if (issued_v[st]) drain_wait(&b.v_full[st], ((issued_v[st] - 1) >> 1) & 1);
@@ -150,51 +304,95 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
 
 // ---------------------------------------------------------------- MMA issuer
 
-template <int D, bool kBf16>
+template <int D, bool kBf16, int G>
 __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem,
-                                         int ntiles) {
+                                         const uint64_t* items, int count) {
   using L = PrefillLayout<D>;
   constexpr uint32_t kIdescQK = idesc_f16(kBf16, kTile, kTile, false, false);
   constexpr uint32_t kIdescPV = idesc_f16(kBf16, kTile, D, false, true);
-  const uint32_t s_tmem = tmem, o_tmem = tmem + kTile;
-  const uint32_t q_addr = smem_u32(smem + L::kQ);
-  const uint32_t p_addr = smem_u32(smem + L::kP);
-  bool ok = mbar_wait(b.q, 0, a.status);
-  bool issued_any = false;
-  for (int j = 0; ok && j <= ntiles; ++j) {
-    if (j < ntiles) {
-      const int st = j & 1, use = j >> 1;
-      if (!mbar_wait(&b.k_full[st], use & 1, a.status)) { ok = false; break; }
-      if (j >= 1 && !mbar_wait(b.s_free, (j - 1) & 1, a.status)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kTileBytes);
+  const uint32_t s_tmem[2] = {tmem, tmem + kTile};
+  const uint32_t o_tmem[2] = {tmem + 2 * kTile, tmem + 3 * kTile};
+  const uint32_t q_addr[2] = {smem_u32(smem + L::kQA), smem_u32(smem + L::kQB)};
+  bool ok = true, issued_any = false;
+  int g = 0, items_done = 0;
+
+  // S_X = Q_X K^T for the key tile in stage st
+  auto qk = [&](int x, int st) {
+    const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kTileBytes);
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t off = (ks >> 2) * L::kRegionBytes + (ks & 3) * 32;
-        umma_f16_ss(s_tmem, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(k_addr + off, 16, 1024),
-                    kIdescQK, ks > 0 ? 1u : 0u);
-      }
-      issued_any = true;
-      umma_commit(b.s_full);
-      umma_commit(&b.k_empty[st]);
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint32_t off = (ks >> 2) * L::kRegionBytes + (ks & 3) * 32;
+      umma_f16_ss(s_tmem[x], smem_desc_sw128(q_addr[x] + off, 16, 1024), smem_desc_sw128(k_addr + off, 16, 1024),
+                  kIdescQK, ks > 0 ? 1u : 0u);
     }
-    if (j >= 1) {
-      const int i = j - 1, st = i & 1, use = i >> 1;
-      if (!mbar_wait(b.p_full, i & 1, a.status)) { ok = false; break; }
-      if (!mbar_wait(&b.v_full[st], use & 1, a.status)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTileBytes);
+    umma_commit(&b.s_full[x]);
+    issued_any = true;
+  };
+  // O_X (+)= P_X V, P_X from TMEM (over S_X), V MN-major: 64-column halves
+  // L::kRegionBytes apart (leading offset), 8-key row groups 1024 B apart
+  auto pv = [&](int x, int st, bool accumulate) {
+    const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTileBytes);
 #pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        const uint64_t pdesc = smem_desc_sw128(p_addr + (kk >> 2) * L::kRegionBytes + (kk & 3) * 32, 16, 1024);
-        // V tile [key][d] is MN-major for O += P V: 64-column halves L::kRegionBytes
-        // apart (leading offset), 8-key row groups 1024 B apart (stride offset)
-        const uint64_t vdesc = smem_desc_sw128(v_addr + kk * 16 * 128, L::kRegionBytes, 1024);
-        umma_f16_ss(o_tmem, pdesc, vdesc, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < kTile / 16; ++kk)
+      umma_f16_ts(o_tmem[x], s_tmem[x] + 8 * kk, smem_desc_sw128(v_addr + kk * 16 * 128, L::kRegionBytes, 1024),
+                  kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+  };
+
+  for (int r = 0; ok; ++r) {
+    const int idx = item_index(r);
+    if (idx >= count) break;
+    const Item it = item_unpack(items[idx]);
+    const PairGeom p = pair_geom<G>(a, it.s, it.pair);
+    const int n = p.ntiles;
+    if (n == 0) continue;
+    if (!mbar_wait(b.q_full, items_done & 1, a.status)) { ok = false; break; }
+    // the previous item's epilogues must have read O_A / O_B before PV overwrites them
+    const bool wait_o = items_done > 0;
+    const int g0 = g;
+    if (!mbar_wait(&b.k_full[g0 & 1], (g0 >> 1) & 1, a.status)) { ok = false; break; }
+    tc_fence_after();
+    qk(0, g0 & 1);
+    qk(1, g0 & 1);
+    umma_commit(&b.k_empty[g0 & 1]);
+    if (n == 1) umma_commit(b.q_empty);
+    for (int j = 0; j < n && ok; ++j) {
+      const int gt = g0 + j, st = gt & 1;
+      // tile A: PV(j), then QK(j + 1)
+      if (!mbar_wait(&b.p_full[0], gt & 1, a.status) || !mbar_wait(&b.v_full[st], (gt >> 1) & 1, a.status) ||
+          (j == 0 && wait_o && !mbar_wait(&b.o_free[0], (items_done - 1) & 1, a.status))) {
+        ok = false;
+        break;
       }
-      umma_commit(b.o_done);
+      tc_fence_after();
+      pv(0, st, j > 0);
+      if (j + 1 < n) {
+        const int st1 = (gt + 1) & 1;
+        if (!mbar_wait(&b.k_full[st1], ((gt + 1) >> 1) & 1, a.status)) { ok = false; break; }
+        tc_fence_after();
+        qk(0, st1);
+      } else {
+        umma_commit(&b.o_full[0]);
+      }
+      // tile B: PV(j), then QK(j + 1)
+      if (!mbar_wait(&b.p_full[1], gt & 1, a.status) ||
+          (j == 0 && wait_o && !mbar_wait(&b.o_free[1], (items_done - 1) & 1, a.status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      pv(1, st, j > 0);
       umma_commit(&b.v_empty[st]);
+      if (j + 1 < n) {
+        const int st1 = (gt + 1) & 1;
+        qk(1, st1);
+        umma_commit(&b.k_empty[st1]);
+        if (j + 2 == n) umma_commit(b.q_empty);
+      } else {
+        umma_commit(&b.o_full[1]);
+      }
     }
+    g += n;
+    ++items_done;
   }
   if (!ok && issued_any) {  // wait for this thread's MMAs before TMEM is released
     umma_commit(b.drain);
@@ -204,72 +402,88 @@ __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const
 
 // ---------------------------------------------------------------- softmax
 
-// A wait whose outcome is the same for all 32 lanes, so that warp-collective
-// instructions after it never run with lanes missing.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
 
 template <int D, bool kBf16, int G>
-__device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem, int q0,
-                                             int t_begin, int ntok, int h, int nkeys, int ntiles) {
+__device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem,
+                                             const uint64_t* items, int count, int x) {
   using L = PrefillLayout<D>;
-  const int r = threadIdx.x;  // row = TMEM lane
-  const int warp = r >> 5;
-  const int tl = r / G, g = r % G;
-  const bool row_valid = tl < ntok;
-  const int tok = q0 + t_begin + min(tl, ntok - 1);
-  const int pos = __ldg(a.positions + tok);
-  const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-  const uint32_t s_tmem = tmem + lane_off, o_tmem = tmem + kTile + lane_off;
-  const uint32_t p_addr = smem_u32(smem + L::kP);
+  constexpr int TQ = kTile / G;
+  // the reference maximum of the exponents is raised only when the row
+  // maximum passes it by more than 2^8 (exp2 units): probabilities stay below
+  // 2^8, well inside fp16/bf16 range, and O / l is unchanged
+  constexpr float kRescaleThreshold = 8.f;
+  const int r = threadIdx.x - kTile * x;  // row of tile x = TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(32 * ((threadIdx.x >> 5) & 3)) << 16;
+  const uint32_t s_tmem = tmem + kTile * x + lane_off;
+  const uint32_t o_tmem = tmem + 2 * kTile + kTile * x + lane_off;
   const float c2 = a.scale_log2;
-  float m = kNegInf, l = 0.f;
+  const int tl = r / G, gg = r % G;
+  int g = 0, items_done = 0;
   bool ok = true;
 
-  for (int j = 0; j < ntiles; ++j) {
-    if (!warp_wait(b.s_full, j & 1, a.status)) { ok = false; break; }
-    tc_fence_after();
-    float sv[kTile];
-#pragma unroll
-    for (int c = 0; c < kTile / 32; ++c) {
-      uint32_t t[32];
-      tmem_ld32(s_tmem + 32 * c, t);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) sv[32 * c + i] = __uint_as_float(t[i]);
-    }
-    tc_fence_before();
-    mbar_arrive(b.s_free);
+  for (int ri = 0; ok; ++ri) {
+    const int idx = item_index(ri);
+    if (idx >= count) break;
+    const Item it = item_unpack(items[idx]);
+    const PairGeom p = pair_geom<G>(a, it.s, it.pair);
+    const int n = p.ntiles;
+    if (n == 0) continue;
+    const int nvalid = x == 0 ? p.n_a : p.n_b;
+    const bool row_valid = tl < nvalid;
+    // rows past the last token compute on whatever the tile holds, at the
+    // position of the pair's last token, and are never stored
+    const int tok = row_valid ? p.q0 + p.tok_a + TQ * x + tl : p.q0 + p.tok_a + p.n_a + p.n_b - 1;
+    const int pos = __ldg(a.positions + tok);
+    float m_ref = kNegInf, l = 0.f;
 
-    // causal mask: key k is visible to this row iff k <= pos
-    const int kb0 = kTile * j;
-    if (kb0 + kTile - 1 > pos) {
-#pragma unroll
-      for (int i = 0; i < kTile; ++i)
-        if (kb0 + i > pos) sv[i] = kNegInf;
-    }
-    float mx = sv[0];
-#pragma unroll
-    for (int i = 1; i < kTile; ++i) mx = fmaxf(mx, sv[i]);
-    const float m_new = fmaxf(m, mx);
-    const float ms = (m_new == kNegInf ? 0.f : m_new) * c2;
-    const float alpha = ex2(fmaf(m, c2, -ms));
-    float sum = 0.f;
-    uint32_t pk[kTile / 2];
-#pragma unroll
-    for (int i = 0; i < kTile / 2; ++i) {
-      const float p0 = ex2(fmaf(sv[2 * i], c2, -ms));
-      const float p1 = ex2(fmaf(sv[2 * i + 1], c2, -ms));
-      sum += p0 + p1;
-      pk[i] = pack2<kBf16>(p0, p1);
-    }
-    l = fmaf(l, alpha, sum);
-    m = m_new;
-
-    if (j > 0) {  // PV of the previous tile must be done before O is rescaled and P rewritten
-      if (!warp_wait(b.o_done, (j - 1) & 1, a.status)) { ok = false; break; }
+    for (int j = 0; j < n; ++j) {
+      const int gt = g + j;
+      if (!warp_wait(&b.s_full[x], gt & 1, a.status)) { ok = false; break; }
       tc_fence_after();
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      float sv[kTile];
+      {
+        uint32_t t[kTile];
+        tmem_ld128(s_tmem, t);
+#pragma unroll
+        for (int i = 0; i < kTile; ++i) sv[i] = __uint_as_float(t[i]);
+      }
+      // causal mask: key k is visible to this row iff k <= pos
+      const int kb0 = kTile * j;
+      if (kb0 + kTile - 1 > pos) {
+#pragma unroll
+        for (int i = 0; i < kTile; ++i)
+          if (kb0 + i > pos) sv[i] = kNegInf;
+      }
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = sv[k];
+#pragma unroll
+      for (int i = 8; i < kTile; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
+      const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const bool raise = m_tile != kNegInf && (m_ref == kNegInf || (m_tile - m_ref) * c2 > kRescaleThreshold);
+      float alpha = 1.f;
+      if (raise) {
+        alpha = ex2((m_ref - m_tile) * c2);  // 0 on the first visible tile
+        m_ref = m_tile;
+      }
+      const float ms = (m_ref == kNegInf ? 0.f : m_ref) * c2;
+      float sums[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[kTile / 2];
+#pragma unroll
+      for (int i = 0; i < kTile / 2; ++i) {
+        const float p0 = ex2(fmaf(sv[2 * i], c2, -ms));
+        const float p1 = ex2(fmaf(sv[2 * i + 1], c2, -ms));
+        sums[i & 7] += p0 + p1;
+        pk[i] = pack2<kBf16>(p0, p1);
+      }
+      l = fmaf(l, alpha, ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7])));
+      // PV of the previous key tile completed before S of this one (same
+      // issuing thread, committed in order), so O can be rescaled here
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t t[32];
@@ -279,38 +493,32 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
           tmem_st32(o_tmem + 32 * c, t);
         }
       }
-    }
-    if (j == ntiles - 1 && nkeys < kb0 + kTile) {
-      // value rows past the last needed key may hold anything (even NaN, or
-      // nothing loaded at all): zero them so that P = 0 contributes 0
-      const int st = j & 1;
-      if (!warp_wait(&b.v_full[st], (j >> 1) & 1, a.status)) { ok = false; break; }
-      if (r >= nkeys - kb0) {
-        const uint32_t vrow = smem_u32(smem + L::kV + st * L::kTileBytes) + r * 128;
+      if (x == 0 && j == n - 1 && p.nkeys < kb0 + kTile) {
+        // value rows past the last needed key may hold anything (even NaN,
+        // or nothing loaded at all): zero them so that P = 0 contributes 0
+        // (tile A's PV, the first to read this stage, waits for p_full[0])
+        const int st = gt & 1;
+        if (!warp_wait(&b.v_full[st], (gt >> 1) & 1, a.status)) { ok = false; break; }
+        if (r >= p.nkeys - kb0) {
+          const uint32_t vrow = smem_u32(smem + L::kV + st * L::kTileBytes) + r * 128;
 #pragma unroll
-        for (int reg = 0; reg < L::kRegions; ++reg)
+          for (int reg = 0; reg < L::kRegions; ++reg)
 #pragma unroll
-          for (int c = 0; c < 8; ++c) st_shared_v4(vrow + reg * L::kRegionBytes + c * 16, 0, 0, 0, 0);
+            for (int c = 0; c < 8; ++c) st_shared_zero16(vrow + reg * L::kRegionBytes + c * 16);
+        }
+        fence_proxy_async_smem();
       }
+      tmem_st64(s_tmem, pk);  // P over the first 64 columns of S
+      tc_fence_before();
+      mbar_arrive(&b.p_full[x]);
     }
-    // P row r, K-major with the 128-byte swizzle: keys 0-63 in region 0, 64-127 in region 1
-#pragma unroll
-    for (int half = 0; half < 2; ++half)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int k = half * 32 + 4 * c;
-        st_shared_v4(p_addr + half * L::kRegionBytes + r * 128 + ((c ^ (r & 7)) << 4), pk[k], pk[k + 1], pk[k + 2],
-                     pk[k + 3]);
-      }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    mbar_arrive(b.p_full);
-  }
-
-  if (ok && ntiles > 0 && warp_wait(b.o_done, (ntiles - 1) & 1, a.status)) {
+    if (!ok) break;
+    g += n;
+    if (!warp_wait(&b.o_full[x], items_done & 1, a.status)) { ok = false; break; }
     tc_fence_after();
     const float inv = 1.f / l;
-    uint16_t* dst = static_cast<uint16_t*>(a.out) + (static_cast<size_t>(tok) * a.num_q_heads + h * G + g) * D;
+    uint16_t* dst =
+        static_cast<uint16_t*>(a.out) + (static_cast<size_t>(tok) * a.num_q_heads + it.h * G + gg) * D;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t t[32];
@@ -325,6 +533,9 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
         for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       }
     }
+    tc_fence_before();
+    mbar_arrive(&b.o_free[x]);
+    ++items_done;
   }
 }
 
@@ -333,50 +544,31 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
 template <int D, bool kBf16, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                   const __grid_constant__ CUtensorMap qmap, const AttnArgs a) {
+                   const __grid_constant__ CUtensorMap qmap, const AttnArgs a, const uint64_t* items,
+                   const int* count_ptr) {
   using L = PrefillLayout<D>;
-  constexpr int TQ = kTile / G;  // tokens per tile
-  const int qt = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
-  const int q0 = __ldg(a.query_start_loc + s);
-  const int qlen = __ldg(a.query_start_loc + s + 1) - q0;
-  if (q0 < 0 || qlen < 0 || q0 + qlen > a.num_tokens) {
-    if (qt == 0 && h == 0 && threadIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
-    return;
-  }
-  if (qlen == 0 || qlen * G <= a.decode_max_rows) return;  // empty, or served by the decode kernel
-  const int t_begin = qt * TQ;
-  if (t_begin >= qlen) return;
-  const int ntok = min(TQ, qlen - t_begin);
-  const int ctx = __ldg(a.context_lens + s);
-  const int pos_last = __ldg(a.positions + q0 + t_begin + ntok - 1);
-  const int pos_first = __ldg(a.positions + q0 + t_begin);
-  if (ctx <= 0 || ctx > a.max_blocks_per_seq * a.block_size || pos_last >= ctx || pos_first < 0 ||
-      pos_first > pos_last) {
-    if (h == 0 && threadIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_POSITION);
-    return;
-  }
-  const int nkeys = pos_last + 1;  // keys 0..pos_last cover every row of the tile
-  const int ntiles = ceil_div(nkeys, kTile);
-
+  const int count = *count_ptr;
+  if (static_cast<int>(blockIdx.x) >= count) return;  // no item for this CTA
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  Bars b{bar, bar + 1, bar + 3, bar + 5, bar + 7, bar + 9, bar + 10, bar + 11, bar + 12, bar + 13};
+  const Bars b{bar, bar + 1, bar + 2, bar + 4, bar + 6, bar + 8, bar + 10, bar + 12, bar + 14, bar + 16, bar + 18};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + L::kNumBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(b.q, 1);
-    for (int st = 0; st < kStages; ++st) {
-      mbar_init(&b.k_full[st], 1);
-      mbar_init(&b.k_empty[st], 1);
-      mbar_init(&b.v_full[st], 1);
-      mbar_init(&b.v_empty[st], 1);
+    mbar_init(b.q_full, 1);
+    mbar_init(b.q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b.k_full[i], 1);
+      mbar_init(&b.k_empty[i], 1);
+      mbar_init(&b.v_full[i], 1);
+      mbar_init(&b.v_empty[i], 1);
+      mbar_init(&b.s_full[i], 1);
+      mbar_init(&b.p_full[i], kTile);
+      mbar_init(&b.o_full[i], 1);
+      mbar_init(&b.o_free[i], kTile);
     }
-    mbar_init(b.s_full, 1);
-    mbar_init(b.s_free, kTile);
-    mbar_init(b.p_full, kTile);
-    mbar_init(b.o_done, 1);
     mbar_init(b.drain, 1);
     fence_mbar_init();
   }
@@ -389,12 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
-    softmax_role<D, kBf16, G>(a, smem, b, tmem, q0, t_begin, ntok, h, nkeys, ntiles);
+  if (warp < 8) {
+    softmax_role<D, kBf16, G>(a, smem, b, tmem, items, count, warp >> 2);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<D, G>(&kmap, &vmap, &qmap, a, smem, b, s, h, q0 + t_begin, nkeys, ntiles);
+    if (lane == 0) producer_role<D, G>(&kmap, &vmap, &qmap, a, smem, b, items, count);
   } else {
-    if (lane == 0) mma_role<D, kBf16>(a, smem, b, tmem, ntiles);
+    if (lane == 0) mma_role<D, kBf16, G>(a, smem, b, tmem, items, count);
   }
   tc_fence_before();
   __syncthreads();
@@ -411,9 +603,10 @@ cudaError_t launch_prefill_t(const AttnArgs& a, const CUtensorMap& kmap, const C
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = set_smem_limit_once(prefill_kernel<D, kBf16, G>, L::kAlloc, configured);
   if (e != cudaSuccess) return e;
-  constexpr int TQ = kTile / G;
-  dim3 grid((a.max_query_len + TQ - 1) / TQ, a.num_kv_heads, a.num_seqs);
-  prefill_kernel<D, kBf16, G><<<grid, kThreads, L::kAlloc, stream>>>(kmap, vmap, qmap, a);
+  prefill_plan_kernel<G><<<1, kPlanThreads, 0, stream>>>(a, a.ws_items, a.ws_item_count, a.max_items);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  prefill_kernel<D, kBf16, G><<<a.sm_count, kThreads, L::kAlloc, stream>>>(kmap, vmap, qmap, a, a.ws_items,
+                                                                            a.ws_item_count);
   return cudaGetLastError();
 }
 
@@ -431,6 +624,12 @@ cudaError_t launch_prefill_g(const AttnArgs& a, const CUtensorMap& kmap, const C
 }
 
 }  // namespace
+
+int prefill_max_items(int num_seqs, int num_tokens, int num_q_heads, int num_kv_heads) {
+  const int G = num_q_heads / num_kv_heads;
+  const int pair_tokens = 2 * (kTile / (G > 0 ? G : 1));
+  return num_kv_heads * ((num_tokens + pair_tokens - 1) / pair_tokens + num_seqs);
+}
 
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            const CUtensorMap& qmap, cudaStream_t stream) {

@@ -121,15 +121,21 @@ def test_attention_with_no_tokens_is_a_noop(lib):
 
 def test_workspace_size_host_only(lib):
     import paged_kv_cache_arena_gb300 as K
-    # a short context needs one split: no partials
-    assert K.kshipra_paged_attention_workspace_size(4, 4, 100, 32, 8, 128, sm_count=152) == 0
+    r256 = lambda x: -(-x // 256) * 256
+    # a short context needs one split: no partials, only the prefill work list
+    # (one 8-byte item per pair of 128-row query tiles per kv head, plus its length)
+    items = 8 * (-(-4 // 64) + 4)
+    assert K.kshipra_paged_attention_workspace_size(4, 4, 100, 32, 8, 128, sm_count=152) == r256(items * 8 + 4)
     big = K.kshipra_paged_attention_workspace_size(16, 16, 32768, 32, 8, 128, sm_count=152)
     assert big > 0 and big % 256 == 0
     K.kshipra_set_option(K.KSHIPRA_OPT_SPLIT_TOKENS, 1024)
     try:
         ws = K.kshipra_paged_attention_workspace_size(16, 16, 32768, 32, 8, 128, sm_count=152)
         splits = 32
-        assert ws == -(-splits * 16 * 32 * 128 * 4 // 256) * 256 + -(-splits * 16 * 32 * 2 * 4 // 256) * 256
+        counters = r256(16 * 8 * 4)  # one finished-split counter per (sequence, kv head)
+        items = 8 * (-(-16 // 64) + 16)
+        assert ws == (r256(splits * 16 * 32 * 128 * 4) + r256(splits * 16 * 32 * 2 * 4) + counters
+                      + r256(items * 8 + 4))
     finally:
         K.kshipra_set_option(K.KSHIPRA_OPT_SPLIT_TOKENS, 0)
     out = ctypes.c_size_t(0)
