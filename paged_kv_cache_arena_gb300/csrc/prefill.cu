@@ -19,22 +19,25 @@
 // sorts them, heaviest first; the persistent attention kernel (one CTA per
 // SM) walks that list in snake order.
 //
-// Roles in the attention kernel (320 threads):
-//  - warp 8 (one lane): TMA producer.  Q_A and Q_B are 3-D boxes (token x head
+// Roles in the attention kernel (576 threads):
+//  - warp 16 (one lane): TMA producer.  Q_A and Q_B are 3-D boxes (token x head
 //    x 64 columns); each K/V tile is 128 / block_size arena-block boxes
 //    addressed through the block table, double-buffered.
-//  - warp 9 (one lane): tcgen05.mma issuer, ping-pong between the tiles:
+//  - warp 17 (one lane): tcgen05.mma issuer, ping-pong between the tiles:
 //    S_X = Q_X K^T (M 128, N 128, K d) into TMEM, then O_X += P_X V (M 128,
 //    N d, K 128) with P_X read from TMEM (written over S_X by the softmax) and
 //    V read MN-major in its arena layout.  While one tile's softmax runs, the
 //    tensor core works on the other tile.
-//  - warps 0-3 / 4-7: softmax of tile A / B.  Thread r owns row r (TMEM lane
-//    r): loads its S row, masks, keeps the running max / sum (the reference
+//  - warps 0-7 / 8-15: softmax of tile A / B.  Two threads own row r (TMEM
+//    lane r), one per 64-key half: each loads its half of the S row, masks,
+//    and they swap partial row maxima through shared memory (a 64-thread
+//    named barrier per warp pair); each keeps a running sum (the reference
 //    max is only raised when the row max passes it by 2^8, so O is rarely
 //    rescaled), writes P as fp16/bf16 back into TMEM, and at the end of the
 //    item normalises O and stores the output row.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+d), O_B [384,384+d);
-// P_X occupies the first 64 columns of S_X.
+// P_X (two 16-bit values per column) occupies columns [0,32) and [64,96) of
+// S_X, the first half of each softmax thread's own 64 S columns.
 // Every wait is bounded (mbar_wait); on a timeout all roles stop, drain their
 // outstanding copies / MMAs and release tensor memory.
 #include <float.h>
@@ -46,9 +49,9 @@ namespace kshipra {
 namespace {
 
 constexpr int kTile = 128;  // query rows per tile and keys per key tile
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 576;  // 16 softmax warps, producer, MMA issuer
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kNegInf = -INFINITY;
@@ -64,7 +67,9 @@ struct PrefillLayout {
   static constexpr int kQB = kQA + kTileBytes;
   static constexpr int kK = kQB + kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBar = kV + kStages * kTileBytes;
+  static constexpr int kX = kV + kStages * kTileBytes;  // row max / sum exchange between half-row threads
+  static constexpr int kXBytes = (2 * 2 * 2 + 2 * 2) * kTile * 4;
+  static constexpr int kBar = kX + kXBytes;
   // q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
   // p_full[2], o_full[2], o_free[2], drain; then the TMEM base address
   static constexpr int kNumBars = 19;
@@ -241,7 +246,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
   const int oob_row = a.num_blocks * a.num_kv_heads * bs;  // past the tensor: zero fill
   int g = 0;                                               // key tiles issued by this CTA
   int items_done = 0;
-  int issued_k[kStages] = {0, 0}, issued_v[kStages] = {0, 0};
+  int issued_k0 = 0, issued_k1 = 0, issued_v0 = 0, issued_v1 = 0;  // last tile + 1 per stage
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = item_index(r);
@@ -266,39 +271,45 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
       const int nb = ceil_div(min(kTile * (j + 1), p.nkeys) - kTile * j, bs);
       const uint32_t bytes = static_cast<uint32_t>(nb * bs * 128 * L::kRegions);
       int rows[kTile / 16];
-      for (int i = 0; i < nb; ++i) {
-        const int blk = __ldg(table + j * blocks_per_tile + i);
-        if (blk < 0 || blk >= a.num_blocks) {
-          report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
-          rows[i] = oob_row;
-        } else {
-          rows[i] = (blk * a.num_kv_heads + it.h) * bs;
+#pragma unroll
+      for (int i = 0; i < kTile / 16; ++i) {
+        rows[i] = oob_row;
+        if (i < nb) {
+          const int blk = __ldg(table + j * blocks_per_tile + i);
+          if (blk < 0 || blk >= a.num_blocks)
+            report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
+          else
+            rows[i] = (blk * a.num_kv_heads + it.h) * bs;
         }
       }
       if (g >= kStages && !mbar_wait(&b.k_empty[st], (use - 1) & 1, a.status)) { ok = false; break; }
       mbar_arrive_expect_tx(&b.k_full[st], bytes);
       uint8_t* kdst = smem + L::kK + st * L::kTileBytes;
-      for (int i = 0; i < nb; ++i)
 #pragma unroll
-        for (int reg = 0; reg < L::kRegions; ++reg)
-          tma_load_2d(kdst + reg * L::kRegionBytes + i * bs * 128, kmap, 64 * reg, rows[i], &b.k_full[st]);
-      issued_k[st] = g + 1;
+      for (int i = 0; i < kTile / 16; ++i)
+        if (i < nb)
+#pragma unroll
+          for (int reg = 0; reg < L::kRegions; ++reg)
+            tma_load_2d(kdst + reg * L::kRegionBytes + i * bs * 128, kmap, 64 * reg, rows[i], &b.k_full[st]);
+      (st ? issued_k1 : issued_k0) = g + 1;
       if (g >= kStages && !mbar_wait(&b.v_empty[st], (use - 1) & 1, a.status)) { ok = false; break; }
       mbar_arrive_expect_tx(&b.v_full[st], bytes);
       uint8_t* vdst = smem + L::kV + st * L::kTileBytes;
-      for (int i = 0; i < nb; ++i)
 #pragma unroll
-        for (int reg = 0; reg < L::kRegions; ++reg)
-          tma_load_2d(vdst + reg * L::kRegionBytes + i * bs * 128, vmap, 64 * reg, rows[i], &b.v_full[st]);
-      issued_v[st] = g + 1;
+      for (int i = 0; i < kTile / 16; ++i)
+        if (i < nb)
+#pragma unroll
+          for (int reg = 0; reg < L::kRegions; ++reg)
+            tma_load_2d(vdst + reg * L::kRegionBytes + i * bs * 128, vmap, 64 * reg, rows[i], &b.v_full[st]);
+      (st ? issued_v1 : issued_v0) = g + 1;
     }
   }
   if (!ok) {  // let every copy this thread started land before the CTA moves on
     if (items_done) drain_wait(b.q_full, (items_done - 1) & 1);
-    for (int st = 0; st < kStages; ++st) {
-      if (issued_k[st]) drain_wait(&b.k_full[st], ((issued_k[st] - 1) >> 1) & 1);
-      if (issued_v[st]) drain_wait(&b.v_full[st], ((issued_v[st] - 1) >> 1) & 1);
-    }
+    if (issued_k0) drain_wait(&b.k_full[0], ((issued_k0 - 1) >> 1) & 1);
+    if (issued_k1) drain_wait(&b.k_full[1], ((issued_k1 - 1) >> 1) & 1);
+    if (issued_v0) drain_wait(&b.v_full[0], ((issued_v0 - 1) >> 1) & 1);
+    if (issued_v1) drain_wait(&b.v_full[1], ((issued_v1 - 1) >> 1) & 1);
   }
 }
 
@@ -310,9 +321,9 @@ __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const
   using L = PrefillLayout<D>;
   constexpr uint32_t kIdescQK = idesc_f16(kBf16, kTile, kTile, false, false);
   constexpr uint32_t kIdescPV = idesc_f16(kBf16, kTile, D, false, true);
-  const uint32_t s_tmem[2] = {tmem, tmem + kTile};
-  const uint32_t o_tmem[2] = {tmem + 2 * kTile, tmem + 3 * kTile};
-  const uint32_t q_addr[2] = {smem_u32(smem + L::kQA), smem_u32(smem + L::kQB)};
+  const uint32_t q_base = smem_u32(smem + L::kQA);  // Q_B follows Q_A
+  auto s_tmem = [&](int x) { return tmem + kTile * x; };
+  auto o_tmem = [&](int x) { return tmem + 2 * kTile + kTile * x; };
   bool ok = true, issued_any = false;
   int g = 0, items_done = 0;
 
@@ -322,19 +333,20 @@ __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       const uint32_t off = (ks >> 2) * L::kRegionBytes + (ks & 3) * 32;
-      umma_f16_ss(s_tmem[x], smem_desc_sw128(q_addr[x] + off, 16, 1024), smem_desc_sw128(k_addr + off, 16, 1024),
+      umma_f16_ss(s_tmem(x), smem_desc_sw128(q_base + x * L::kTileBytes + off, 16, 1024), smem_desc_sw128(k_addr + off, 16, 1024),
                   kIdescQK, ks > 0 ? 1u : 0u);
     }
     umma_commit(&b.s_full[x]);
     issued_any = true;
   };
-  // O_X (+)= P_X V, P_X from TMEM (over S_X), V MN-major: 64-column halves
-  // L::kRegionBytes apart (leading offset), 8-key row groups 1024 B apart
+  // O_X (+)= P_X V, P_X from TMEM over S_X (keys 16 kk.. of step kk in
+  // columns 8 kk (kk < 4) or 8 kk + 32 (kk >= 4)), V MN-major: 64-column
+  // halves L::kRegionBytes apart (leading offset), 8-key row groups 1024 B apart
   auto pv = [&](int x, int st, bool accumulate) {
     const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTileBytes);
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk)
-      umma_f16_ts(o_tmem[x], s_tmem[x] + 8 * kk, smem_desc_sw128(v_addr + kk * 16 * 128, L::kRegionBytes, 1024),
+      umma_f16_ts(o_tmem(x), s_tmem(x) + 8 * kk + (kk >= 4 ? 32 : 0), smem_desc_sw128(v_addr + kk * 16 * 128, L::kRegionBytes, 1024),
                   kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
   };
 
@@ -406,19 +418,33 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
 
+// Named barrier for the two warps that share a row range (same TMEM lanes).
+__device__ __forceinline__ void pair_sync(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+
+// Each row of tile x is handled by two threads: `half` 0 takes key columns
+// 0-63 (and O columns 0..d/2-1), half 1 the other halves.  They exchange
+// their partial row maxima every key tile and their partial sums at the end.
 template <int D, bool kBf16, int G>
 __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem,
-                                             const uint64_t* items, int count, int x) {
+                                             const uint64_t* items, int count, int x, int half) {
   using L = PrefillLayout<D>;
   constexpr int TQ = kTile / G;
+  constexpr int HC = kTile / 2;  // key columns per thread
+  constexpr int HD = D / 2;      // O columns per thread
   // the reference maximum of the exponents is raised only when the row
   // maximum passes it by more than 2^8 (exp2 units): probabilities stay below
   // 2^8, well inside fp16/bf16 range, and O / l is unchanged
   constexpr float kRescaleThreshold = 8.f;
-  const int r = threadIdx.x - kTile * x;  // row of tile x = TMEM lane
-  const uint32_t lane_off = static_cast<uint32_t>(32 * ((threadIdx.x >> 5) & 3)) << 16;
+  const int quarter = (threadIdx.x >> 5) & 3;
+  const int r = 32 * quarter + (threadIdx.x & 31);  // row of tile x = TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
   const uint32_t s_tmem = tmem + kTile * x + lane_off;
-  const uint32_t o_tmem = tmem + 2 * kTile + kTile * x + lane_off;
+  const uint32_t o_tmem = tmem + 2 * kTile + kTile * x + lane_off + HD * half;
+  const int bar_id = 1 + 4 * x + quarter;
+  float* xmax = reinterpret_cast<float*>(smem + L::kX) + x * 2 * 2 * kTile;  // [parity][half][row]
+  float* xsum = reinterpret_cast<float*>(smem + L::kX) + 2 * 2 * 2 * kTile + x * 2 * kTile;  // [half][row]
   const float c2 = a.scale_log2;
   const int tl = r / G, gg = r % G;
   int g = 0, items_done = 0;
@@ -443,27 +469,30 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
       const int gt = g + j;
       if (!warp_wait(&b.s_full[x], gt & 1, a.status)) { ok = false; break; }
       tc_fence_after();
-      float sv[kTile];
+      // pass 1: the half row's maximum over visible keys
+      const int kb0 = kTile * j + HC * half;
+      const bool diag = kb0 + HC - 1 > pos;  // some keys of this half are past the row's position
+      float m_tile;
       {
-        uint32_t t[kTile];
-        tmem_ld128(s_tmem, t);
+        float mx[8];
 #pragma unroll
-        for (int i = 0; i < kTile; ++i) sv[i] = __uint_as_float(t[i]);
+        for (int k = 0; k < 8; ++k) mx[k] = kNegInf;
+#pragma unroll
+        for (int cc = 0; cc < HC / 32; ++cc) {
+          uint32_t t[32];
+          tmem_ld32(s_tmem + HC * half + 32 * cc, t);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float v = (diag && kb0 + 32 * cc + i > pos) ? kNegInf : __uint_as_float(t[i]);
+            mx[i & 7] = fmaxf(mx[i & 7], v);
+          }
+        }
+        m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       }
-      // causal mask: key k is visible to this row iff k <= pos
-      const int kb0 = kTile * j;
-      if (kb0 + kTile - 1 > pos) {
-#pragma unroll
-        for (int i = 0; i < kTile; ++i)
-          if (kb0 + i > pos) sv[i] = kNegInf;
-      }
-      float mx[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = sv[k];
-#pragma unroll
-      for (int i = 8; i < kTile; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
-      const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      float* xm = xmax + (gt & 1) * 2 * kTile;
+      xm[half * kTile + r] = m_tile;
+      pair_sync(bar_id);
+      m_tile = fmaxf(m_tile, xm[(1 - half) * kTile + r]);  // both halves now hold the row maximum
       const bool raise = m_tile != kNegInf && (m_ref == kNegInf || (m_tile - m_ref) * c2 > kRescaleThreshold);
       float alpha = 1.f;
       if (raise) {
@@ -471,21 +500,35 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
         m_ref = m_tile;
       }
       const float ms = (m_ref == kNegInf ? 0.f : m_ref) * c2;
-      float sums[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[kTile / 2];
+      // pass 2, 32 keys at a time: probabilities, their sum, and P (two per
+      // column) written over this half's own, already read, S columns:
+      // keys 32 cc + [0, 32) of half h go to columns 64 h + 16 cc + [0, 16)
+      float sums[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < kTile / 2; ++i) {
-        const float p0 = ex2(fmaf(sv[2 * i], c2, -ms));
-        const float p1 = ex2(fmaf(sv[2 * i + 1], c2, -ms));
-        sums[i & 7] += p0 + p1;
-        pk[i] = pack2<kBf16>(p0, p1);
+      for (int cc = 0; cc < HC / 32; ++cc) {
+        uint32_t t[32];
+        tmem_ld32(s_tmem + HC * half + 32 * cc, t);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int k0 = kb0 + 32 * cc + 2 * i;
+          float p0 = ex2(fmaf(__uint_as_float(t[2 * i]), c2, -ms));
+          float p1 = ex2(fmaf(__uint_as_float(t[2 * i + 1]), c2, -ms));
+          if (diag) {
+            p0 = k0 > pos ? 0.f : p0;
+            p1 = k0 + 1 > pos ? 0.f : p1;
+          }
+          sums[i & 3] += p0 + p1;
+          pk[i] = pack2<kBf16>(p0, p1);
+        }
+        tmem_st16(s_tmem + HC * half + 16 * cc, pk);
       }
-      l = fmaf(l, alpha, ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7])));
+      l = fmaf(l, alpha, (sums[0] + sums[1]) + (sums[2] + sums[3]));
       // PV of the previous key tile completed before S of this one (same
       // issuing thread, committed in order), so O can be rescaled here
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < HD / 32; ++c) {
           uint32_t t[32];
           tmem_ld32(o_tmem + 32 * c, t);
 #pragma unroll
@@ -493,34 +536,34 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
           tmem_st32(o_tmem + 32 * c, t);
         }
       }
-      if (x == 0 && j == n - 1 && p.nkeys < kb0 + kTile) {
+      if (x == 0 && j == n - 1 && p.nkeys < kTile * j + kTile && half < L::kRegions) {
         // value rows past the last needed key may hold anything (even NaN,
         // or nothing loaded at all): zero them so that P = 0 contributes 0
         // (tile A's PV, the first to read this stage, waits for p_full[0])
         const int st = gt & 1;
         if (!warp_wait(&b.v_full[st], (gt >> 1) & 1, a.status)) { ok = false; break; }
-        if (r >= p.nkeys - kb0) {
-          const uint32_t vrow = smem_u32(smem + L::kV + st * L::kTileBytes) + r * 128;
+        if (r >= p.nkeys - kTile * j) {
+          const uint32_t vrow = smem_u32(smem + L::kV + st * L::kTileBytes) + half * L::kRegionBytes + r * 128;
 #pragma unroll
-          for (int reg = 0; reg < L::kRegions; ++reg)
-#pragma unroll
-            for (int c = 0; c < 8; ++c) st_shared_zero16(vrow + reg * L::kRegionBytes + c * 16);
+          for (int c = 0; c < 8; ++c) st_shared_zero16(vrow + c * 16);
         }
         fence_proxy_async_smem();
       }
-      tmem_st64(s_tmem, pk);  // P over the first 64 columns of S
       tc_fence_before();
       mbar_arrive(&b.p_full[x]);
     }
     if (!ok) break;
     g += n;
+    xsum[half * kTile + r] = l;
+    pair_sync(bar_id);
+    l += xsum[(1 - half) * kTile + r];
     if (!warp_wait(&b.o_full[x], items_done & 1, a.status)) { ok = false; break; }
     tc_fence_after();
     const float inv = 1.f / l;
-    uint16_t* dst =
-        static_cast<uint16_t*>(a.out) + (static_cast<size_t>(tok) * a.num_q_heads + it.h * G + gg) * D;
+    uint16_t* dst = static_cast<uint16_t*>(a.out) +
+                    (static_cast<size_t>(tok) * a.num_q_heads + it.h * G + gg) * D + HD * half;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < HD / 32; ++c) {
       uint32_t t[32];
       tmem_ld32(o_tmem + 32 * c, t);
       uint32_t w[16];
@@ -535,6 +578,7 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
     }
     tc_fence_before();
     mbar_arrive(&b.o_free[x]);
+    pair_sync(bar_id);  // the partner has read xsum before it is written again
     ++items_done;
   }
 }
@@ -565,9 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b.v_full[i], 1);
       mbar_init(&b.v_empty[i], 1);
       mbar_init(&b.s_full[i], 1);
-      mbar_init(&b.p_full[i], kTile);
+      mbar_init(&b.p_full[i], 2 * kTile);
       mbar_init(&b.o_full[i], 1);
-      mbar_init(&b.o_free[i], kTile);
+      mbar_init(&b.o_free[i], 2 * kTile);
     }
     mbar_init(b.drain, 1);
     fence_mbar_init();
@@ -581,8 +625,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 8) {
-    softmax_role<D, kBf16, G>(a, smem, b, tmem, items, count, warp >> 2);
+  if (warp < 16) {
+    softmax_role<D, kBf16, G>(a, smem, b, tmem, items, count, warp >> 3, (warp >> 2) & 1);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role<D, G>(&kmap, &vmap, &qmap, a, smem, b, items, count);
   } else {
