@@ -96,14 +96,15 @@ size_t kshipra_kv_bytes_per_token(int num_layers, int num_kv_heads, int head_dim
 
 /*
  * RoPE table on the host: host_out[p][i][0] = cos(p * theta^(-2i/d)),
- * host_out[p][i][1] = sin(...), for p < max_pos, i < head_dim / 2, in
- * float64 (rotate-half convention: element i pairs with i + d/2).
+ * host_out[p][i][1] = sin(...), for p < max_pos, i < head_dim / 2
+ * (rotate-half convention: element i pairs with i + d/2).  The angle, cos and
+ * sin are evaluated in float64 and each entry is rounded once to float32.
  * (kshipra-3, section 4: RoPE uses absolute positions.)  The caller copies it
  * to the device once and passes that copy to kshipra_kv_append_rope.
- * host_out must hold max_pos * head_dim entries.  Host only, no CUDA calls.
+ * host_out must hold max_pos * head_dim floats.  Host only, no CUDA calls.
  * Errors: INVALID_ARG (null, max_pos < 0, head_dim odd or < 2, theta <= 0).
  */
-int kshipra_rope_table_build(double* host_out, int max_pos, int head_dim, double theta);
+int kshipra_rope_table_build(float* host_out, int max_pos, int head_dim, double theta);
 
 /*
  * RoPE and append (kshipra-3, sections 1 and 4).  For every token t of
@@ -114,15 +115,16 @@ int kshipra_rope_table_build(double* host_out, int max_pos, int head_dim, double
  *   - k_arena[b][h][p % block_size] = RoPE(k[t][h], p) and
  *     v_arena[b][h][p % block_size] = v[t][h] for every kv head, where
  *     b = block_tables[s][p / block_size].
- * The rotation is computed in float64 from rope_table (separate products,
- * then one add) and rounded once to dtype (nearest, ties to even), so the
- * arena contents are reproducible bit for bit.  V rows are copied bit for
+ * The rotation is computed in float32 from rope_table (two separately
+ * rounded products, then one rounded add or subtract; no fused multiply-add)
+ * and rounded once to dtype (nearest, ties to even), so the arena contents
+ * are reproducible bit for bit.  V rows are copied bit for
  * bit.  q_rot may alias q.  Other arena slots are not touched.
  *
  * q, q_rot [num_tokens][num_q_heads][head_dim]; k, v [num_tokens]
  * [num_kv_heads][head_dim]; k_arena, v_arena, block_tables, query_start_loc
  * [num_seqs + 1], positions [num_tokens], rope_table [rope_max_pos]
- * [head_dim/2][2] float64: all device pointers.
+ * [head_dim/2][2] float32: all device pointers.
  * Device-side violations: a block id outside [0, num_blocks), a logical block
  * index >= max_blocks_per_seq or a position outside [0, rope_max_pos) skip
  * that token's writes and set KSHIPRA_DEV_BAD_BLOCK_ID / _BAD_POSITION.
@@ -130,7 +132,7 @@ int kshipra_rope_table_build(double* host_out, int max_pos, int head_dim, double
  */
 int kshipra_kv_append_rope(const void* q, const void* k, const void* v, void* q_rot, void* k_arena,
                            void* v_arena, const int32_t* block_tables, const int32_t* query_start_loc,
-                           const int32_t* positions, const double* rope_table, int rope_max_pos, int num_seqs,
+                           const int32_t* positions, const float* rope_table, int rope_max_pos, int num_seqs,
                            int num_tokens, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                            int max_blocks_per_seq, int num_blocks, int dtype, void* stream);
 

@@ -18,9 +18,11 @@
  * Readings where the pages are silent (each is listed in the design notes):
  *  - RoPE pairs element i with i + d/2 ("rotate half"), frequency
  *    theta^(-2i/d), angle = position * frequency, float64 libm cos/sin.
- *  - The rotated key stored in the arena is the float64 rotation rounded once
- *    (nearest, ties to even) to the storage type; products are formed
- *    separately and then added (no fused multiply-add).
+ *  - Attention uses the exact float64 rotation.  The rotated key stored in the
+ *    arena (and the stored q_rot) is the float32 rotation: cos/sin rounded to
+ *    float32, separately rounded float32 products, one float32 add or
+ *    subtract (no fused multiply-add), then one rounding (nearest, ties to
+ *    even) to the storage type.
  *  - scale is a caller input (1/sqrt(d) in every workload).
  *
  * Nothing here is shared with the CUDA library: conversions, RoPE and the
@@ -157,19 +159,36 @@ static void rope_row(const double* x, double* y, long pos, int d, double theta) 
     }
 }
 
+/* The stored rotation (arena keys and q_rot): cos and sin from the float64
+ * angle rounded once to float32, the pair rotated with separately rounded
+ * float32 products and one float32 add/subtract (built without contraction),
+ * then rounded once to the storage type by the caller. */
+static void rope_row_f32(const float* x, float* y, long pos, int d, double theta) {
+    int h = d / 2;
+    for (int i = 0; i < h; ++i) {
+        double c, s;
+        rope_angle(pos, i, d, theta, &c, &s);
+        float cf = (float)c, sf = (float)s;
+        float a = x[i], b = x[i + h];
+        float ac = a * cf, bs = b * sf, bc = b * cf, as = a * sf;
+        y[i] = ac - bs;
+        y[i + h] = bc + as;
+    }
+}
+
 /* Expected bits of rotated rows: rows[n][H][d] at positions pos[n], rounded
  * once to the storage type.  Used for q_rot and for the rotated keys. */
 int oracle_rope_rows(const uint16_t* rows, uint16_t* out, const int32_t* pos, long n, int H, int d,
                      double theta, int dtype) {
     if (d <= 0 || (d & 1) || d > 1024) return 1;
-    double x[1024], y[1024];
+    float x[1024], y[1024];
     for (long t = 0; t < n; ++t)
         for (int hh = 0; hh < H; ++hh) {
             const uint16_t* r = rows + ((size_t)t * H + hh) * d;
-            for (int i = 0; i < d; ++i) x[i] = to_f64(r[i], dtype);
-            rope_row(x, y, pos[t], d, theta);
+            for (int i = 0; i < d; ++i) x[i] = (float)to_f64(r[i], dtype);
+            rope_row_f32(x, y, pos[t], d, theta);
             uint16_t* o = out + ((size_t)t * H + hh) * d;
-            for (int i = 0; i < d; ++i) o[i] = from_f64(y[i], dtype);
+            for (int i = 0; i < d; ++i) o[i] = from_f64((double)y[i], dtype);
         }
     return 0;
 }
@@ -188,7 +207,7 @@ int oracle_arena_image(uint16_t* k_arena, uint16_t* v_arena, const uint16_t* k_r
                        const int32_t* block_tables, int max_blocks_per_seq, int num_blocks, int Hkv, int bs,
                        int d, double theta, int dtype) {
     if (d <= 0 || (d & 1) || d > 1024) return 1;
-    double x[1024], y[1024];
+    float x[1024], y[1024];
     for (int s = 0; s < num_seqs; ++s)
         for (int t = query_start_loc[s]; t < query_start_loc[s + 1]; ++t) {
             long p = positions[t];
@@ -199,9 +218,9 @@ int oracle_arena_image(uint16_t* k_arena, uint16_t* v_arena, const uint16_t* k_r
             for (int h = 0; h < Hkv; ++h) {
                 size_t src = ((size_t)t * Hkv + h) * d;
                 size_t dst = (((size_t)blk * Hkv + h) * bs + slot) * d;
-                for (int i = 0; i < d; ++i) x[i] = to_f64(k_rows[src + i], dtype);
-                rope_row(x, y, p, d, theta);
-                for (int i = 0; i < d; ++i) k_arena[dst + i] = from_f64(y[i], dtype);
+                for (int i = 0; i < d; ++i) x[i] = (float)to_f64(k_rows[src + i], dtype);
+                rope_row_f32(x, y, p, d, theta);
+                for (int i = 0; i < d; ++i) k_arena[dst + i] = from_f64((double)y[i], dtype);
                 memcpy(v_arena + dst, v_rows + src, (size_t)d * sizeof(uint16_t));
             }
         }

@@ -79,8 +79,8 @@ def kshipra_kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int
 
 
 def kshipra_rope_table_build(max_pos: int, head_dim: int, theta: float) -> np.ndarray:
-    """Host float64 table [max_pos, head_dim/2, 2] of (cos, sin)."""
-    out = np.empty((max_pos, head_dim // 2, 2), dtype=np.float64)
+    """Host float32 table [max_pos, head_dim/2, 2] of (cos, sin)."""
+    out = np.empty((max_pos, head_dim // 2, 2), dtype=np.float32)
     _check(_lib.load().kshipra_rope_table_build(ctypes.c_void_p(out.ctypes.data), max_pos, head_dim, float(theta)),
            "kshipra_rope_table_build")
     return out

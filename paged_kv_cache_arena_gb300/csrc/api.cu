@@ -210,7 +210,7 @@ size_t kshipra_kv_bytes_per_token(int num_layers, int num_kv_heads, int head_dim
   return 2 * static_cast<size_t>(num_layers) * num_kv_heads * head_dim * elem;
 }
 
-int kshipra_rope_table_build(double* host_out, int max_pos, int head_dim, double theta) {
+int kshipra_rope_table_build(float* host_out, int max_pos, int head_dim, double theta) {
   if (!host_out) return fail(KSHIPRA_ERR_INVALID_ARG, "host_out is NULL");
   if (max_pos < 0 || head_dim < 2 || (head_dim & 1) || !(theta > 0.0))
     return fail(KSHIPRA_ERR_INVALID_ARG, "bad rope table shape (max_pos %d, head_dim %d, theta %g)", max_pos,
@@ -220,8 +220,8 @@ int kshipra_rope_table_build(double* host_out, int max_pos, int head_dim, double
     const double inv_freq = std::pow(theta, -2.0 * i / head_dim);
     for (long p = 0; p < max_pos; ++p) {
       const double angle = static_cast<double>(p) * inv_freq;
-      host_out[(p * half + i) * 2] = std::cos(angle);
-      host_out[(p * half + i) * 2 + 1] = std::sin(angle);
+      host_out[(p * half + i) * 2] = static_cast<float>(std::cos(angle));
+      host_out[(p * half + i) * 2 + 1] = static_cast<float>(std::sin(angle));
     }
   }
   return KSHIPRA_OK;
@@ -273,7 +273,7 @@ int kshipra_device_status(int32_t* code_out, void* stream) {
 
 int kshipra_kv_append_rope(const void* q, const void* k, const void* v, void* q_rot, void* k_arena,
                            void* v_arena, const int32_t* block_tables, const int32_t* query_start_loc,
-                           const int32_t* positions, const double* rope_table, int rope_max_pos, int num_seqs,
+                           const int32_t* positions, const float* rope_table, int rope_max_pos, int num_seqs,
                            int num_tokens, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                            int max_blocks_per_seq, int num_blocks, int dtype, void* stream) {
   g_last_error[0] = 0;

@@ -7,9 +7,10 @@
 // and section 4 (RoPE at absolute positions: a chunk after P cached tokens
 // starts at position P).
 //
-// One warp per (token, head).  The rotation is done in float64 from the caller's
-// (cos, sin) table with separate products and one add, then rounded once to
-// the storage type, so the arena image is reproducible bit for bit.  The
+// One warp per (token, head).  The rotation is done in float32 from the
+// caller's (cos, sin) table with separately rounded products and one add,
+// then rounded once to the storage type, so the arena image is reproducible
+// bit for bit.  (float32 keeps the step off GB300's slow FP64 units.)  The
 // volume is small (num_tokens x (Hq + Hkv) x head_dim elements per call); the
 // kernel is memory-latency bound and far from the hot path's cost.
 #include "common.cuh"
@@ -21,28 +22,35 @@ namespace {
 constexpr int kAppendWarps = 4;
 constexpr int kAppendThreads = 32 * kAppendWarps;
 
-// Rotates pairs (i, i + d/2) and (i + 1, i + 1 + d/2) of one head row.
+// Storage bits -> float32 (exact).
+template <bool kBf16>
+__device__ __forceinline__ float bits_to_float(uint32_t h) {
+  if constexpr (kBf16)
+    return __uint_as_float(h << 16);
+  else
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// Rotates pairs (i, i + d/2) and (i + 1, i + 1 + d/2) of one head row:
+//   y_i = x_i c - x_{i+d/2} s,  y_{i+d/2} = x_{i+d/2} c + x_i s
+// with separately rounded float32 products and one rounded add or subtract,
+// then one rounding to the storage type.
 template <bool kBf16>
 __device__ __forceinline__ void rotate_two_pairs(const uint16_t* src, uint16_t* dst, int i, int half,
-                                                 const double* cs) {
+                                                 const float* cs) {
   const uint32_t lo = *reinterpret_cast<const uint32_t*>(src + i);
   const uint32_t hi = *reinterpret_cast<const uint32_t*>(src + i + half);
-  const double2 t01 = *reinterpret_cast<const double2*>(cs + 2 * i);      // c_i, s_i
-  const double2 t23 = *reinterpret_cast<const double2*>(cs + 2 * i + 2);  // c_i+1, s_i+1
-    const double x0 = bits_to_double<kBf16>(static_cast<uint16_t>(lo & 0xFFFF));
-  const double x1 = bits_to_double<kBf16>(static_cast<uint16_t>(lo >> 16));
-  const double y0 = bits_to_double<kBf16>(static_cast<uint16_t>(hi & 0xFFFF));
-  const double y1 = bits_to_double<kBf16>(static_cast<uint16_t>(hi >> 16));
-  const double a0 = __dsub_rn(__dmul_rn(x0, t01.x), __dmul_rn(y0, t01.y));
-  const double b0 = __dadd_rn(__dmul_rn(y0, t01.x), __dmul_rn(x0, t01.y));
-  const double a1 = __dsub_rn(__dmul_rn(x1, t23.x), __dmul_rn(y1, t23.y));
-  const double b1 = __dadd_rn(__dmul_rn(y1, t23.x), __dmul_rn(x1, t23.y));
-  const uint32_t olo = static_cast<uint32_t>(double_to_bits<kBf16>(a0)) |
-                       (static_cast<uint32_t>(double_to_bits<kBf16>(a1)) << 16);
-  const uint32_t ohi = static_cast<uint32_t>(double_to_bits<kBf16>(b0)) |
-                       (static_cast<uint32_t>(double_to_bits<kBf16>(b1)) << 16);
-  *reinterpret_cast<uint32_t*>(dst + i) = olo;
-  *reinterpret_cast<uint32_t*>(dst + i + half) = ohi;
+  const float4 t = *reinterpret_cast<const float4*>(cs + 2 * i);  // c_i, s_i, c_i+1, s_i+1
+  const float x0 = bits_to_float<kBf16>(lo & 0xFFFF), x1 = bits_to_float<kBf16>(lo >> 16);
+  const float y0 = bits_to_float<kBf16>(hi & 0xFFFF), y1 = bits_to_float<kBf16>(hi >> 16);
+  const float a0 = __fsub_rn(__fmul_rn(x0, t.x), __fmul_rn(y0, t.y));
+  const float b0 = __fadd_rn(__fmul_rn(y0, t.x), __fmul_rn(x0, t.y));
+  const float a1 = __fsub_rn(__fmul_rn(x1, t.z), __fmul_rn(y1, t.w));
+  const float b1 = __fadd_rn(__fmul_rn(y1, t.z), __fmul_rn(x1, t.w));
+  *reinterpret_cast<uint32_t*>(dst + i) =
+      static_cast<uint32_t>(round_f32<kBf16>(a0)) | (static_cast<uint32_t>(round_f32<kBf16>(a1)) << 16);
+  *reinterpret_cast<uint32_t*>(dst + i + half) =
+      static_cast<uint32_t>(round_f32<kBf16>(b0)) | (static_cast<uint32_t>(round_f32<kBf16>(b1)) << 16);
 }
 
 // One warp per (token, head): warps of blockIdx.y cover q heads first, then
@@ -74,7 +82,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendArgs 
     return;
   }
   const int D = a.head_dim, half = D / 2;
-  const double* cs = a.rope_table + static_cast<size_t>(pos) * D;  // [d/2][2] for this position
+  const float* cs = a.rope_table + static_cast<size_t>(pos) * D;  // [d/2][2] for this position
   const int i = 2 * lane;                                           // first pair of this lane
   if (hh < nq) {
     const size_t row = (static_cast<size_t>(t) * a.num_q_heads + hh) * D;

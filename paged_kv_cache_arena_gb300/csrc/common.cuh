@@ -1,6 +1,6 @@
 // Shared device helpers for the sm_103a kernels: shared-memory barriers, TMA
-// loads, warp-level matrix loads / MMA, tcgen05 (TMEM) wrappers, IEEE
-// rounding from double, and the device status word.  Inline PTX written from
+// loads, warp-level matrix loads / MMA, tcgen05 (TMEM) wrappers and the
+// device status word.  Inline PTX written from
 // the PTX ISA; no library kernels.
 #pragma once
 
@@ -359,57 +359,6 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
       "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]),
       "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
       : "memory");
-}
-
-// ---------------------------------------------------------------- IEEE
-
-// Storage bits -> double (exact).
-template <bool kBf16>
-__device__ __forceinline__ double bits_to_double(uint16_t h) {
-  if constexpr (kBf16) {
-    return static_cast<double>(__uint_as_float(static_cast<uint32_t>(h) << 16));
-  } else {
-    return static_cast<double>(__half2float(__ushort_as_half(h)));
-  }
-}
-
-// double -> storage bits with a single rounding (nearest, ties to even),
-// written with integer operations on the IEEE encoding.  EB exponent bits,
-// MB fraction bits of the target format.
-template <int EB, int MB>
-__device__ __forceinline__ uint16_t double_to_small(double x) {
-  const uint64_t b = static_cast<uint64_t>(__double_as_longlong(x));
-  const uint32_t sign = static_cast<uint32_t>(b >> 63) << (EB + MB);
-  const uint64_t mag = b & 0x7FFFFFFFFFFFFFFFull;
-  constexpr int kExpAllOnes = (1 << EB) - 1;
-  constexpr int kBias = (1 << (EB - 1)) - 1;
-  if (mag >= 0x7FF0000000000000ull) {  // infinity or NaN
-    const uint32_t frac = mag > 0x7FF0000000000000ull ? (1u << (MB - 1)) : 0u;
-    return static_cast<uint16_t>(sign | (kExpAllOnes << MB) | frac);
-  }
-  const int dexp = static_cast<int>(mag >> 52);
-  if (dexp == 0) return static_cast<uint16_t>(sign);  // zero / double subnormal
-  const int texp = dexp - 1023 + kBias;               // biased exponent in the target
-  if (texp >= kExpAllOnes) return static_cast<uint16_t>(sign | (kExpAllOnes << MB));
-  const uint64_t sig = (mag & 0x000FFFFFFFFFFFFFull) | 0x0010000000000000ull;
-  const int drop = texp >= 1 ? 52 - MB : 52 - MB + 1 - texp;  // low bits removed
-  if (drop >= 54) return static_cast<uint16_t>(sign);
-  uint64_t kept = sig >> drop;
-  const uint64_t rest = sig & ((1ull << drop) - 1);
-  const uint64_t halfway = 1ull << (drop - 1);
-  kept += (rest > halfway || (rest == halfway && (kept & 1))) ? 1 : 0;
-  // normal: kept still holds the hidden bit, so (texp - 1) << MB + kept adds
-  // it into the exponent field; a rounding carry moves up one binade.
-  const uint64_t enc = texp >= 1 ? (static_cast<uint64_t>(texp - 1) << MB) + kept : kept;
-  return static_cast<uint16_t>(sign | static_cast<uint32_t>(enc));
-}
-
-template <bool kBf16>
-__device__ __forceinline__ uint16_t double_to_bits(double x) {
-  if constexpr (kBf16)
-    return double_to_small<8, 7>(x);
-  else
-    return double_to_small<5, 10>(x);
 }
 
 // ---------------------------------------------------------------- host

@@ -23,7 +23,7 @@ struct AppendArgs {
   const int32_t* block_tables;
   const int32_t* query_start_loc;
   const int32_t* positions;
-  const double* rope_table;
+  const float* rope_table;
   int rope_max_pos;
   int num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks;
   int dtype;

@@ -160,13 +160,33 @@ def test_rope_one_hot_rows_give_table_entries(oracle_mod):
         rows[i, 0, i] = one  # e_i
     pos = np.full(d // 2, 7, np.int32)
     out = oracle_mod.bits_to_f64(oracle_mod.rope_rows(rows, pos, theta, "f16"), "f16")
-    tab = oracle_mod.rope_table(8, d, theta)[7]
+    tab = oracle_mod.rope_table(8, d, theta)[7].astype(np.float32)  # stored rotations use float32 cos/sin
     for i in range(d // 2):
         # rotating e_i gives (cos) at i and (+sin) at i + d/2, nothing else
         assert out[i, 0, i] == np.float16(tab[i, 0])
         assert out[i, 0, i + d // 2] == np.float16(tab[i, 1])
         rest = np.delete(out[i, 0], [i, i + d // 2])
         assert np.all(rest == 0)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_stored_rotation_is_one_rounding_from_exact(oracle_mod, dtype):
+    # the stored (float32-computed) rotation differs from the exact rotation by
+    # at most half a storage ulp plus the float32 error (a few 2^-24 relative)
+    rng = np.random.default_rng(8)
+    d, theta = 64, 1.0e4
+    conv = {"f16": lambda a: a.astype(np.float16).view(np.uint16),
+            "bf16": lambda a: ((a.astype(np.float32).view(np.uint32) + 0x8000) >> 16).astype(np.uint16)}[dtype]
+    rows = conv(rng.standard_normal((200, 1, d)))
+    pos = rng.integers(0, 5000, 200).astype(np.int32)
+    got = oracle_mod.bits_to_f64(oracle_mod.rope_rows(rows, pos, theta, dtype), dtype)[:, 0]
+    x = oracle_mod.bits_to_f64(rows, dtype)[:, 0]
+    unit = 2.0 ** -11 if dtype == "f16" else 2.0 ** -8
+    for t in range(200):
+        exact = brute.rotate(list(x[t]), int(pos[t]), theta)
+        for i in range(d):
+            e = abs(got[t, i] - exact[i])
+            assert e <= unit * abs(exact[i]) + 4 * 2.0 ** -24 * (abs(x[t, i]) + abs(x[t, (i + d // 2) % d])) + 1e-30
 
 
 def _rot_f64(x, p, tab_row):
