@@ -43,9 +43,9 @@ struct AttnArgs {
   float* ws_o;   // [max_splits][num_tokens][num_q_heads][head_dim] partial accumulators
   float* ws_ml;  // [max_splits][num_tokens][num_q_heads][2] partial (max, sum)
   unsigned* ws_counters;  // [num_seqs][num_kv_heads] finished splits, zeroed by the host each call
-  uint64_t* ws_items;     // prefill work list (written by the planning kernel)
-  int* ws_item_count;
-  int max_items;          // capacity of ws_items
+  uint64_t* ws_items;     // prefill (sequence, tile pair) entries, written by the planning kernel
+  int* ws_item_count;     // work items = entries x num_kv_heads
+  int max_items;          // capacity of ws_items (entries)
   int sm_count;           // CTAs of the persistent prefill kernel
   unsigned* status;
   int num_seqs, num_tokens, max_query_len, max_context_len;
@@ -61,8 +61,8 @@ struct AttnArgs {
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
 
-// Upper bound on the prefill work items of a call (pairs of 128-row query
-// tiles per (sequence, kv head)).
+// Upper bound on the prefill work-list entries of a call (pairs of 128-row
+// query tiles per sequence).
 int prefill_max_items(int num_seqs, int num_tokens, int num_q_heads, int num_kv_heads);
 
 // Chunked prefill on tcgen05 / TMEM: planning kernel, then the persistent

@@ -55,8 +55,6 @@ constexpr int kMmaWarp = 17;
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kNegInf = -INFINITY;
-constexpr int kPlanThreads = 1024;
-constexpr int kSortCapacity = 4096;  // items sorted in shared memory; longer lists keep plan order
 
 template <int D>
 struct PrefillLayout {
@@ -108,21 +106,22 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsign
 
 // ---------------------------------------------------------------- work items
 //
-// item = cost (16 bits) | sequence (24) | tile pair (16) | kv head (8); sorting
-// the 64-bit values in descending order puts the most expensive items first.
+// The planning kernel lists one entry per (sequence, tile pair): cost (key
+// tiles, 16 bits) | sequence (24) | tile pair (16); sorting the 64-bit values
+// in descending order puts the most expensive first.  Work item i is entry
+// i / Hkv for kv head i % Hkv (the cost does not depend on the head).
 
-__host__ __device__ constexpr uint64_t item_pack(uint32_t cost, uint32_t s, uint32_t pair, uint32_t h) {
-  return (static_cast<uint64_t>(cost) << 48) | (static_cast<uint64_t>(s) << 24) |
-         (static_cast<uint64_t>(pair) << 8) | h;
+__host__ __device__ constexpr uint64_t entry_pack(uint32_t cost, uint32_t s, uint32_t pair) {
+  return (static_cast<uint64_t>(cost) << 40) | (static_cast<uint64_t>(s) << 16) | pair;
 }
 
 struct Item {
   int s, pair, h;
 };
 
-__device__ __forceinline__ Item item_unpack(uint64_t v) {
-  return Item{static_cast<int>((v >> 24) & 0xFFFFFF), static_cast<int>((v >> 8) & 0xFFFF),
-              static_cast<int>(v & 0xFF)};
+__device__ __forceinline__ Item item_at(const uint64_t* entries, int i, int num_kv_heads) {
+  const uint64_t v = entries[i / num_kv_heads];
+  return Item{static_cast<int>((v >> 16) & 0xFFFFFF), static_cast<int>(v & 0xFFFF), i % num_kv_heads};
 }
 
 // Index of this CTA's r-th item (snake order over the sorted list).
@@ -158,16 +157,21 @@ __device__ __forceinline__ PairGeom pair_geom(const AttnArgs& a, int s, int pair
   return p;
 }
 
-// Lists the prefill items (sequences with query_len x group rows above the
-// decode threshold), sorts them by cost and writes them to items[]; *count
-// receives their number.  One CTA.
+// Lists one entry per (prefill sequence, tile pair) -- sequences with
+// query_len x group rows above the decode threshold -- sorts them by cost
+// (rank sort, entries are distinct) and writes them to entries[]; *count
+// receives entries x num_kv_heads, the number of work items.  One CTA.
+constexpr int kPlanThreads = 256;
+constexpr int kSortCapacity = 1024;  // longer lists keep plan order
+
 template <int G>
-__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const AttnArgs a, uint64_t* items,
-                                                                     int* count, int max_items) {
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const AttnArgs a, uint64_t* entries,
+                                                                     int* count, int max_entries) {
   constexpr int TQ = kTile / G;
   __shared__ uint64_t buf[kSortCapacity];
-  __shared__ int scan[kPlanThreads];
+  __shared__ int warp_total[kPlanThreads / 32];
   __shared__ int base;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) base = 0;
   __syncthreads();
   for (int s0 = 0; s0 < a.num_seqs; s0 += kPlanThreads) {
@@ -179,55 +183,41 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const AttnAr
       if (q0 >= 0 && qlen > 0 && q0 + qlen <= a.num_tokens && qlen * G > a.decode_max_rows)
         pairs = ceil_div(ceil_div(qlen, TQ), 2);
     }
-    const int n = pairs * a.num_kv_heads;
-    scan[threadIdx.x] = n;
-    __syncthreads();
-    for (int off = 1; off < kPlanThreads; off <<= 1) {  // inclusive scan
-      const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
-      __syncthreads();
-      scan[threadIdx.x] += v;
-      __syncthreads();
+    int incl = pairs;  // inclusive scan within the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
     }
-    int out = base + scan[threadIdx.x] - n;
-    for (int p = 0; p < pairs; ++p) {
+    if (lane == 31) warp_total[warp] = incl;
+    __syncthreads();
+    int before = base;
+    for (int w = 0; w < warp; ++w) before += warp_total[w];
+    int out = before + incl - pairs;
+    for (int p = 0; p < pairs; ++p, ++out) {
       const int last = min(qlen, (2 * p + 2) * TQ) - 1;
       const int nkeys = __ldg(a.positions + q0 + last) + 1;
       const uint32_t cost = static_cast<uint32_t>(min(max(ceil_div(nkeys, kTile), 0), 0xFFFF));
-      for (int h = 0; h < a.num_kv_heads; ++h, ++out) {
-        if (out >= max_items) continue;
-        const uint64_t v = item_pack(cost, s, p, h);
-        if (out < kSortCapacity) buf[out] = v;
-        items[out] = v;
-      }
+      if (out >= max_entries) continue;
+      const uint64_t v = entry_pack(cost, s, p);
+      if (out < kSortCapacity) buf[out] = v;
+      entries[out] = v;
     }
     __syncthreads();
-    if (threadIdx.x == kPlanThreads - 1) base += scan[threadIdx.x];
+    if (threadIdx.x == 0)
+      for (int w = 0; w < kPlanThreads / 32; ++w) base += warp_total[w];
     __syncthreads();
   }
-  const int total = min(base, max_items);
-  if (total <= kSortCapacity) {  // bitonic sort, descending, padded with zeros
-    int n2 = 1;
-    while (n2 < total) n2 <<= 1;
-    for (int i = total + threadIdx.x; i < n2; i += kPlanThreads) buf[i] = 0;
-    __syncthreads();
-    for (int k = 2; k <= n2; k <<= 1)
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = threadIdx.x; i < n2; i += kPlanThreads) {
-          const int l = i ^ j;
-          if (l > i) {
-            const uint64_t x = buf[i], y = buf[l];
-            const bool desc = (i & k) == 0;
-            if (desc ? x < y : x > y) {
-              buf[i] = y;
-              buf[l] = x;
-            }
-          }
-        }
-        __syncthreads();
-      }
-    for (int i = threadIdx.x; i < total; i += kPlanThreads) items[i] = buf[i];
+  const int total = min(base, max_entries);
+  if (total <= kSortCapacity) {
+    for (int i = threadIdx.x; i < total; i += kPlanThreads) {
+      const uint64_t v = buf[i];
+      int rank = 0;
+      for (int k = 0; k < total; ++k) rank += buf[k] > v;
+      entries[rank] = v;
+    }
   }
-  if (threadIdx.x == 0) *count = total;
+  if (threadIdx.x == 0) *count = total * a.num_kv_heads;
 }
 
 // ---------------------------------------------------------------- producer
@@ -251,7 +241,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
   for (int r = 0; ok; ++r) {
     const int idx = item_index(r);
     if (idx >= count) break;
-    const Item it = item_unpack(items[idx]);
+    const Item it = item_at(items, idx, a.num_kv_heads);
     const PairGeom p = pair_geom<G>(a, it.s, it.pair);
     if (p.ntiles == 0) {
       report(a.status, KSHIPRA_DEV_BAD_POSITION);
@@ -353,7 +343,7 @@ __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const
   for (int r = 0; ok; ++r) {
     const int idx = item_index(r);
     if (idx >= count) break;
-    const Item it = item_unpack(items[idx]);
+    const Item it = item_at(items, idx, a.num_kv_heads);
     const PairGeom p = pair_geom<G>(a, it.s, it.pair);
     const int n = p.ntiles;
     if (n == 0) continue;
@@ -453,7 +443,7 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
   for (int ri = 0; ok; ++ri) {
     const int idx = item_index(ri);
     if (idx >= count) break;
-    const Item it = item_unpack(items[idx]);
+    const Item it = item_at(items, idx, a.num_kv_heads);
     const PairGeom p = pair_geom<G>(a, it.s, it.pair);
     const int n = p.ntiles;
     if (n == 0) continue;
@@ -469,9 +459,10 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
       const int gt = g + j;
       if (!warp_wait(&b.s_full[x], gt & 1, a.status)) { ok = false; break; }
       tc_fence_after();
-      // pass 1: the half row's maximum over visible keys
+      // pass 1: the half row's maximum over visible keys.  Only tiles that
+      // cross some row's position (warp-uniform test) pay for the mask.
       const int kb0 = kTile * j + HC * half;
-      const bool diag = kb0 + HC - 1 > pos;  // some keys of this half are past the row's position
+      const bool diag = __any_sync(0xffffffffu, kb0 + HC - 1 > pos);
       float m_tile;
       {
         float mx[8];
@@ -481,10 +472,13 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
         for (int cc = 0; cc < HC / 32; ++cc) {
           uint32_t t[32];
           tmem_ld32(s_tmem + HC * half + 32 * cc, t);
+          if (diag) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float v = (diag && kb0 + 32 * cc + i > pos) ? kNegInf : __uint_as_float(t[i]);
-            mx[i & 7] = fmaxf(mx[i & 7], v);
+            for (int i = 0; i < 32; ++i)
+              mx[i & 7] = fmaxf(mx[i & 7], kb0 + 32 * cc + i > pos ? kNegInf : __uint_as_float(t[i]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(t[i]));
           }
         }
         m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
@@ -509,17 +503,23 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
         uint32_t t[32];
         tmem_ld32(s_tmem + HC * half + 32 * cc, t);
         uint32_t pk[16];
+        if (diag) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int k0 = kb0 + 32 * cc + 2 * i;
-          float p0 = ex2(fmaf(__uint_as_float(t[2 * i]), c2, -ms));
-          float p1 = ex2(fmaf(__uint_as_float(t[2 * i + 1]), c2, -ms));
-          if (diag) {
-            p0 = k0 > pos ? 0.f : p0;
-            p1 = k0 + 1 > pos ? 0.f : p1;
+          for (int i = 0; i < 16; ++i) {
+            const int k0 = kb0 + 32 * cc + 2 * i;
+            const float p0 = k0 > pos ? 0.f : ex2(fmaf(__uint_as_float(t[2 * i]), c2, -ms));
+            const float p1 = k0 + 1 > pos ? 0.f : ex2(fmaf(__uint_as_float(t[2 * i + 1]), c2, -ms));
+            sums[i & 3] += p0 + p1;
+            pk[i] = pack2<kBf16>(p0, p1);
           }
-          sums[i & 3] += p0 + p1;
-          pk[i] = pack2<kBf16>(p0, p1);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(__uint_as_float(t[2 * i]), c2, -ms));
+            const float p1 = ex2(fmaf(__uint_as_float(t[2 * i + 1]), c2, -ms));
+            sums[i & 3] += p0 + p1;
+            pk[i] = pack2<kBf16>(p0, p1);
+          }
         }
         tmem_st16(s_tmem + HC * half + 16 * cc, pk);
       }
@@ -670,9 +670,9 @@ cudaError_t launch_prefill_g(const AttnArgs& a, const CUtensorMap& kmap, const C
 }  // namespace
 
 int prefill_max_items(int num_seqs, int num_tokens, int num_q_heads, int num_kv_heads) {
-  const int G = num_q_heads / num_kv_heads;
+  const int G = num_q_heads / (num_kv_heads > 0 ? num_kv_heads : 1);
   const int pair_tokens = 2 * (kTile / (G > 0 ? G : 1));
-  return num_kv_heads * ((num_tokens + pair_tokens - 1) / pair_tokens + num_seqs);
+  return (num_tokens + pair_tokens - 1) / pair_tokens + num_seqs;  // (sequence, tile pair) entries
 }
 
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,

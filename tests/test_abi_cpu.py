@@ -123,8 +123,8 @@ def test_workspace_size_host_only(lib):
     import paged_kv_cache_arena_gb300 as K
     r256 = lambda x: -(-x // 256) * 256
     # a short context needs one split: no partials, only the prefill work list
-    # (one 8-byte item per pair of 128-row query tiles per kv head, plus its length)
-    items = 8 * (-(-4 // 64) + 4)
+    # (one 8-byte entry per pair of 128-row query tiles per sequence, plus its length)
+    items = -(-4 // 64) + 4
     assert K.kshipra_paged_attention_workspace_size(4, 4, 100, 32, 8, 128, sm_count=152) == r256(items * 8 + 4)
     big = K.kshipra_paged_attention_workspace_size(16, 16, 32768, 32, 8, 128, sm_count=152)
     assert big > 0 and big % 256 == 0
@@ -133,7 +133,7 @@ def test_workspace_size_host_only(lib):
         ws = K.kshipra_paged_attention_workspace_size(16, 16, 32768, 32, 8, 128, sm_count=152)
         splits = 32
         counters = r256(16 * 8 * 4)  # one finished-split counter per (sequence, kv head)
-        items = 8 * (-(-16 // 64) + 16)
+        items = -(-16 // 64) + 16
         assert ws == (r256(splits * 16 * 32 * 128 * 4) + r256(splits * 16 * 32 * 2 * 4) + counters
                       + r256(items * 8 + 4))
     finally:
