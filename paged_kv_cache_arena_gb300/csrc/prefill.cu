@@ -305,40 +305,63 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
 
 // ---------------------------------------------------------------- MMA issuer
 
+// Descriptor words of the tiles the MMA issuer streams over.  The low word
+// carries the start address (16-byte units), so stepping along a tile adds a
+// constant to it; the high word (stride offset, version, swizzle) is fixed.
+struct Descs {
+  uint32_t q_lo[2], k_lo[2], v_lo[2];  // per query tile / per stage
+  uint32_t qk_hi, v_hi;
+};
+
+__device__ __forceinline__ uint32_t lo_word(uint64_t d) { return static_cast<uint32_t>(d); }
+__device__ __forceinline__ uint32_t hi_word(uint64_t d) { return static_cast<uint32_t>(d >> 32); }
+
+// S_x = Q_x K^T for the key tile in stage st, then signal s_full[x].
+template <int D, bool kBf16>
+__device__ __forceinline__ void issue_qk(const Descs& dd, const Bars& b, uint32_t tmem, int x, int st) {
+  using L = PrefillLayout<D>;
+  constexpr uint32_t kIdescQK = idesc_f16(kBf16, kTile, kTile, false, false);
+  const uint32_t q_lo = x ? dd.q_lo[1] : dd.q_lo[0];
+  const uint32_t k_lo = st ? dd.k_lo[1] : dd.k_lo[0];
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const uint32_t off = ((ks >> 2) * L::kRegionBytes + (ks & 3) * 32) >> 4;
+    umma_f16_ss_w(tmem + kTile * x, q_lo + off, dd.qk_hi, k_lo + off, dd.qk_hi, kIdescQK, ks > 0 ? 1u : 0u);
+  }
+  umma_commit(&b.s_full[x]);
+}
+
+// O_x (+)= P_x V.  P_x is read from TMEM over S_x: keys 16 kk.. of step kk in
+// columns 8 kk (kk < 4) or 8 kk + 32 (kk >= 4).  V is MN-major: 64-column
+// halves L::kRegionBytes apart (leading offset), 8-key row groups 1024 B
+// apart (stride offset).
+template <int D, bool kBf16>
+__device__ __forceinline__ void issue_pv(const Descs& dd, uint32_t tmem, int x, int st, bool accumulate) {
+  constexpr uint32_t kIdescPV = idesc_f16(kBf16, kTile, D, false, true);
+  const uint32_t v_lo = st ? dd.v_lo[1] : dd.v_lo[0];
+  const uint32_t acc = accumulate ? 1u : 0u;
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    umma_f16_ts_w(tmem + 2 * kTile + kTile * x, tmem + kTile * x + 8 * kk + (kk >= 4 ? 32 : 0),
+                  v_lo + ((kk * 16 * 128) >> 4), dd.v_hi, kIdescPV, kk > 0 ? 1u : acc);
+}
+
 template <int D, bool kBf16, int G>
 __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem,
                                          const uint64_t* items, int count) {
   using L = PrefillLayout<D>;
-  constexpr uint32_t kIdescQK = idesc_f16(kBf16, kTile, kTile, false, false);
-  constexpr uint32_t kIdescPV = idesc_f16(kBf16, kTile, D, false, true);
-  const uint32_t q_base = smem_u32(smem + L::kQA);  // Q_B follows Q_A
-  auto s_tmem = [&](int x) { return tmem + kTile * x; };
-  auto o_tmem = [&](int x) { return tmem + 2 * kTile + kTile * x; };
+  const uint32_t sb = smem_u32(smem);
+  Descs dd;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    dd.q_lo[i] = lo_word(smem_desc_sw128(sb + L::kQA + i * L::kTileBytes, 16, 1024));
+    dd.k_lo[i] = lo_word(smem_desc_sw128(sb + L::kK + i * L::kTileBytes, 16, 1024));
+    dd.v_lo[i] = lo_word(smem_desc_sw128(sb + L::kV + i * L::kTileBytes, L::kRegionBytes, 1024));
+  }
+  dd.qk_hi = hi_word(smem_desc_sw128(sb, 16, 1024));
+  dd.v_hi = hi_word(smem_desc_sw128(sb, L::kRegionBytes, 1024));
   bool ok = true, issued_any = false;
   int g = 0, items_done = 0;
-
-  // S_X = Q_X K^T for the key tile in stage st
-  auto qk = [&](int x, int st) {
-    const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kTileBytes);
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      const uint32_t off = (ks >> 2) * L::kRegionBytes + (ks & 3) * 32;
-      umma_f16_ss(s_tmem(x), smem_desc_sw128(q_base + x * L::kTileBytes + off, 16, 1024), smem_desc_sw128(k_addr + off, 16, 1024),
-                  kIdescQK, ks > 0 ? 1u : 0u);
-    }
-    umma_commit(&b.s_full[x]);
-    issued_any = true;
-  };
-  // O_X (+)= P_X V, P_X from TMEM over S_X (keys 16 kk.. of step kk in
-  // columns 8 kk (kk < 4) or 8 kk + 32 (kk >= 4)), V MN-major: 64-column
-  // halves L::kRegionBytes apart (leading offset), 8-key row groups 1024 B apart
-  auto pv = [&](int x, int st, bool accumulate) {
-    const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTileBytes);
-#pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk)
-      umma_f16_ts(o_tmem(x), s_tmem(x) + 8 * kk + (kk >= 4 ? 32 : 0), smem_desc_sw128(v_addr + kk * 16 * 128, L::kRegionBytes, 1024),
-                  kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-  };
 
   for (int r = 0; ok; ++r) {
     const int idx = item_index(r);
@@ -353,8 +376,9 @@ __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const
     const int g0 = g;
     if (!mbar_wait(&b.k_full[g0 & 1], (g0 >> 1) & 1, a.status)) { ok = false; break; }
     tc_fence_after();
-    qk(0, g0 & 1);
-    qk(1, g0 & 1);
+    issue_qk<D, kBf16>(dd, b, tmem, 0, g0 & 1);
+    issue_qk<D, kBf16>(dd, b, tmem, 1, g0 & 1);
+    issued_any = true;
     umma_commit(&b.k_empty[g0 & 1]);
     if (n == 1) umma_commit(b.q_empty);
     for (int j = 0; j < n && ok; ++j) {
@@ -366,12 +390,12 @@ __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const
         break;
       }
       tc_fence_after();
-      pv(0, st, j > 0);
+      issue_pv<D, kBf16>(dd, tmem, 0, st, j > 0);
       if (j + 1 < n) {
         const int st1 = (gt + 1) & 1;
         if (!mbar_wait(&b.k_full[st1], ((gt + 1) >> 1) & 1, a.status)) { ok = false; break; }
         tc_fence_after();
-        qk(0, st1);
+        issue_qk<D, kBf16>(dd, b, tmem, 0, st1);
       } else {
         umma_commit(&b.o_full[0]);
       }
@@ -382,11 +406,11 @@ __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const
         break;
       }
       tc_fence_after();
-      pv(1, st, j > 0);
+      issue_pv<D, kBf16>(dd, tmem, 1, st, j > 0);
       umma_commit(&b.v_empty[st]);
       if (j + 1 < n) {
         const int st1 = (gt + 1) & 1;
-        qk(1, st1);
+        issue_qk<D, kBf16>(dd, b, tmem, 1, st1);
         umma_commit(&b.k_empty[st1]);
         if (j + 2 == n) umma_commit(b.q_empty);
       } else {
