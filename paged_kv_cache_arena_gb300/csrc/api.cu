@@ -155,8 +155,14 @@ int check_arena(int num_blocks, int num_kv_heads, int block_size, int max_blocks
 }
 
 // Keys per decode split.  Aims at roughly kDecodeWaves waves of two CTAs per
-// SM for the largest batch these arguments allow; multiples of 64 keys.
-constexpr int kDecodeWaves = 8;
+// SM for the largest batch these arguments allow, in multiples of 64 keys
+// between 256 and kDecodeMaxSplit.  Each split pays a pipeline fill and a
+// partial write, so a few long splits per sequence beat many short ones as
+// long as the grid still covers the GPU several times (on GB300, a 64 x 8
+// head batch at contexts up to 4096 is fastest near 1.5-2 K keys per split,
+// 16 x 32 K contexts near 4-8 K).
+constexpr int kDecodeWaves = 4;
+constexpr int kDecodeMaxSplit = 4096;
 
 int split_tokens_for(int num_seqs, int max_context_len, int num_kv_heads, int sm_count) {
   const int opt = g_opt_split_tokens.load();
@@ -166,6 +172,7 @@ int split_tokens_for(int num_seqs, int max_context_len, int num_kv_heads, int sm
   long long L = (static_cast<long long>(max_context_len) * units + target - 1) / target;
   L = (L + 63) / 64 * 64;
   if (L < 256) L = 256;
+  if (L > kDecodeMaxSplit) L = kDecodeMaxSplit;
   const long long cap = (static_cast<long long>(max_context_len) + 63) / 64 * 64;
   if (L > cap) L = cap < 64 ? 64 : cap;
   return static_cast<int>(L);
