@@ -70,4 +70,9 @@ int prefill_max_items(int num_seqs, int num_tokens, int num_q_heads, int num_kv_
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            const CUtensorMap& qmap, cudaStream_t stream);
 
+// The same for head_dim 128 on CTA pairs (tcgen05 cta_group::2): planning
+// kernel, then the persistent pair kernel.
+cudaError_t launch_prefill_pair(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                const CUtensorMap& qmap, cudaStream_t stream);
+
 }  // namespace kshipra

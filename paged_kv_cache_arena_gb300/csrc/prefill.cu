@@ -702,10 +702,8 @@ int prefill_max_items(int num_seqs, int num_tokens, int num_q_heads, int num_kv_
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                            const CUtensorMap& qmap, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.max_query_len * a.group <= a.decode_max_rows) return cudaSuccess;
+  if (a.head_dim == 128) return launch_prefill_pair(a, kmap, vmap, qmap, stream);
   const bool bf = a.dtype == KSHIPRA_DTYPE_BF16;
-  if (a.head_dim == 128)
-    return bf ? launch_prefill_g<128, true>(a, kmap, vmap, qmap, stream)
-              : launch_prefill_g<128, false>(a, kmap, vmap, qmap, stream);
   return bf ? launch_prefill_g<64, true>(a, kmap, vmap, qmap, stream)
             : launch_prefill_g<64, false>(a, kmap, vmap, qmap, stream);
 }

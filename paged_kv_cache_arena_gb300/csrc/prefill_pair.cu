@@ -1,0 +1,768 @@
+// Chunked-prefill attention over the block arena on CTA pairs (tcgen05
+// cta_group::2), head_dim 128.
+//
+// Pages "Building Kshipra" part 3 (kshipra-3), section 4: a prompt chunk of
+// new tokens sits at absolute positions after the cached prefix; each query
+// attends to the cached prefix and to the earlier tokens of its own chunk
+// (causal mask); attention runs an online softmax over KV blocks read in
+// place from the arena.  Section 1: keys of position p live in slot
+// p % block_size of physical block block_tables[s][p / block_size].
+//
+// Query tiles: 128 rows = 128/G consecutive tokens x the G query heads of one
+// kv head (GQA packing).  A work item is a quad of adjacent query tiles of
+// one (sequence, kv head), run by a cluster of two CTAs on neighbouring SMs:
+// CTA r holds tiles 4q + 2r (its "A") and 4q + 2r + 1 (its "B").  The leader
+// CTA issues M = 256 MMAs that cover both CTAs' A rows (or B rows) at once,
+// so every 128-key K/V tile serves 512 query rows while each SM stages only
+// half of it: CTA r loads keys 64r .. 64r+63 of each K tile (the columns of
+// S split between the pair) and columns 64r .. 64r+63 of each V tile (the
+// columns of O).  Loading K/V from L2 is what bounds a one-CTA version of
+// this kernel on GB300; halving it per SM leaves the tensor core as the
+// limit.
+//
+// Roles (576 threads per CTA):
+//  - warp 16 (one lane): TMA producer.  Q_A / Q_B as 3-D boxes (token x head
+//    x 64 columns); this CTA's halves of each K/V tile as arena-block boxes
+//    through the block table, four stages.  Completion is counted on the
+//    leader's barriers, except the last V tile of an item, which completes on
+//    a barrier of its own CTA so the softmax warps can zero its tail.
+//  - warp 17 (one lane, leader only): MMA issuer, ping-pong between A and B:
+//    S_X = Q_X K^T (M 256, N 128, K 128) into TMEM, then O_X += P_X V
+//    (M 256, N 128, K 128) with P_X read from TMEM, written there over S_X by
+//    the softmax.  Commits arrive on both CTAs' barriers.
+//  - warps 0-7 / 8-15: softmax of tile A / B of their own CTA, two threads per
+//    row (one per 64-key half), exactly as in the one-CTA kernel; each warp
+//    reports "P ready" / "O read" to the leader with one remote arrival.
+// TMEM (each CTA): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// Every wait is bounded; on a timeout all roles stop and drain their own
+// outstanding copies / MMAs before the pair releases tensor memory.
+#include <float.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kshipra {
+namespace {
+
+constexpr int kTile = 128;  // query rows per tile and keys per key tile
+constexpr int kD = 128;
+constexpr int kThreads = 576;
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kStages = 4;  // power of two
+constexpr uint32_t kTmemCols = 512;
+constexpr float kNegInf = -INFINITY;
+
+struct Layout {
+  static constexpr int kQRegion = kTile * 128;  // 128 rows x 64 columns (128-byte swizzle)
+  static constexpr int kQTile = 2 * kQRegion;   // 32 KB
+  static constexpr int kKRegion = 64 * 128;     // this CTA's 64 keys x 64 columns
+  static constexpr int kKStage = 2 * kKRegion;  // 16 KB
+  static constexpr int kVStage = kTile * 128;   // 128 keys x this CTA's 64 columns, 16 KB
+  static constexpr int kQA = 0;
+  static constexpr int kQB = kQA + kQTile;
+  static constexpr int kK = kQB + kQTile;
+  static constexpr int kV = kK + kStages * kKStage;
+  static constexpr int kX = kV + kStages * kVStage;  // row max / sum exchange between half-row threads
+  static constexpr int kXBytes = (2 * 2 * 2 + 2 * 2) * kTile * 4;
+  static constexpr int kBar = kX + kXBytes;
+  static constexpr int kNumBars = 2 + 2 * kStages + 1 + 8 + 1;
+  static constexpr int kBytes = kBar + kNumBars * 8 + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+struct Bars {
+  uint64_t* q_full;   // leader: both CTAs' Q tiles landed
+  uint64_t* q_empty;  // both: the item's last QK MMAs completed
+  uint64_t* kv_full;   // [kStages] leader: both CTAs' K (and V, but for an item's last tile) landed
+  uint64_t* kv_empty;  // [kStages] both: the stage's last PV MMA completed
+  uint64_t* v_last;   // own CTA: the item's last V tile landed in this CTA
+  uint64_t* s_full;   // [2] both
+  uint64_t* p_full;   // [2] leader, 16 warp arrivals (8 per CTA)
+  uint64_t* o_full;   // [2] both
+  uint64_t* o_free;   // [2] leader, 16 warp arrivals
+  uint64_t* drain;    // leader
+};
+
+__device__ __forceinline__ Bars bars_at(uint8_t* smem) {
+  uint64_t* p = reinterpret_cast<uint64_t*>(smem + Layout::kBar);
+  Bars b;
+  b.q_full = p;
+  b.q_empty = p + 1;
+  b.kv_full = p + 2;
+  b.kv_empty = b.kv_full + kStages;
+  b.v_last = b.kv_empty + kStages;
+  b.s_full = b.v_last + 1;
+  b.p_full = b.s_full + 2;
+  b.o_full = b.p_full + 2;
+  b.o_free = b.o_full + 2;
+  b.drain = b.o_free + 2;
+  return b;
+}
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity) && globaltimer() - t0 < kWaitLimitNs) {
+  }
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
+// ---------------------------------------------------------------- work items
+//
+// One entry per (sequence, quad of query tiles): cost (key tiles, 16 bits) |
+// sequence (24) | quad (16); descending order puts the heaviest first.  Work
+// item i is entry i / Hkv for kv head i % Hkv.  Cluster c takes items
+// c, 2C-1-c, 2C+c, ... (snake order over C clusters).
+
+__host__ __device__ constexpr uint64_t entry_pack(uint32_t cost, uint32_t s, uint32_t quad) {
+  return (static_cast<uint64_t>(cost) << 40) | (static_cast<uint64_t>(s) << 16) | quad;
+}
+
+struct Item {
+  int s, quad, h;
+};
+
+__device__ __forceinline__ Item item_at(const uint64_t* entries, int i, int num_kv_heads) {
+  const uint64_t v = entries[i / num_kv_heads];
+  return Item{static_cast<int>((v >> 16) & 0xFFFFFF), static_cast<int>(v & 0xFFFF), i % num_kv_heads};
+}
+
+__device__ __forceinline__ int item_index(int r) {
+  const int nc = gridDim.x >> 1, c = blockIdx.x >> 1;
+  return r * nc + ((r & 1) ? nc - 1 - c : c);
+}
+
+struct QuadGeom {
+  int q0;        // first token of the sequence
+  int tok;       // first token (sequence-relative) of this CTA's tile A
+  int n_a, n_b;  // valid tokens in this CTA's tiles A and B (either may be 0)
+  int last;      // last token (sequence-relative) of the quad
+  int nkeys;     // keys 0..nkeys-1 cover every row of the quad
+  int ntiles;    // 128-key tiles (0 when the item's lengths are inconsistent)
+};
+
+// Both CTAs of a pair compute the same nkeys / ntiles: they walk the same
+// key tiles.
+template <int G>
+__device__ __forceinline__ QuadGeom quad_geom(const AttnArgs& a, int s, int quad, int rank) {
+  constexpr int TQ = kTile / G;
+  QuadGeom p{};
+  p.q0 = __ldg(a.query_start_loc + s);
+  const int qlen = __ldg(a.query_start_loc + s + 1) - p.q0;
+  const int quad_tok = 4 * TQ * quad;
+  p.tok = quad_tok + 2 * TQ * rank;
+  p.n_a = max(0, min(TQ, qlen - p.tok));
+  p.n_b = max(0, min(TQ, qlen - p.tok - TQ));
+  p.last = min(qlen, quad_tok + 4 * TQ) - 1;
+  const int ctx = __ldg(a.context_lens + s);
+  const bool shape_ok = p.q0 >= 0 && p.q0 + qlen <= a.num_tokens && quad_tok < qlen;
+  const int pos_first = shape_ok ? __ldg(a.positions + p.q0 + quad_tok) : -1;
+  const int pos_last = shape_ok ? __ldg(a.positions + p.q0 + p.last) : -1;
+  const bool ok = shape_ok && ctx > 0 && ctx <= a.max_blocks_per_seq * a.block_size && pos_first >= 0 &&
+                  pos_first <= pos_last && pos_last < ctx;
+  p.nkeys = ok ? pos_last + 1 : 0;
+  p.ntiles = ceil_div(p.nkeys, kTile);
+  return p;
+}
+
+// Lists one entry per (prefill sequence, quad) -- sequences with query_len x
+// group rows above the decode threshold -- sorts them by cost (rank sort,
+// entries are distinct) and writes them to entries[]; *count receives
+// entries x num_kv_heads.  One CTA.
+constexpr int kPlanThreads = 256;
+constexpr int kSortCapacity = 1024;  // longer lists keep plan order
+
+template <int G>
+__global__ void __launch_bounds__(kPlanThreads) prefill_pair_plan_kernel(const AttnArgs a, uint64_t* entries,
+                                                                          int* count, int max_entries) {
+  constexpr int TQ = kTile / G;
+  __shared__ uint64_t buf[kSortCapacity];
+  __shared__ int warp_total[kPlanThreads / 32];
+  __shared__ int base;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) base = 0;
+  __syncthreads();
+  for (int s0 = 0; s0 < a.num_seqs; s0 += kPlanThreads) {
+    const int s = s0 + threadIdx.x;
+    int quads = 0, q0 = 0, qlen = 0;
+    if (s < a.num_seqs) {
+      q0 = __ldg(a.query_start_loc + s);
+      qlen = __ldg(a.query_start_loc + s + 1) - q0;
+      if (q0 >= 0 && qlen > 0 && q0 + qlen <= a.num_tokens && qlen * G > a.decode_max_rows)
+        quads = ceil_div(qlen, 4 * TQ);
+    }
+    int incl = quads;  // inclusive scan within the warp
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_total[warp] = incl;
+    __syncthreads();
+    int before = base;
+    for (int w = 0; w < warp; ++w) before += warp_total[w];
+    int out = before + incl - quads;
+    for (int q = 0; q < quads; ++q, ++out) {
+      const int last = min(qlen, 4 * TQ * (q + 1)) - 1;
+      const int nkeys = __ldg(a.positions + q0 + last) + 1;
+      const uint32_t cost = static_cast<uint32_t>(min(max(ceil_div(nkeys, kTile), 0), 0xFFFF));
+      if (out >= max_entries) continue;
+      const uint64_t v = entry_pack(cost, s, q);
+      if (out < kSortCapacity) buf[out] = v;
+      entries[out] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (int w = 0; w < kPlanThreads / 32; ++w) base += warp_total[w];
+    __syncthreads();
+  }
+  const int total = min(base, max_entries);
+  if (total <= kSortCapacity) {
+    for (int i = threadIdx.x; i < total; i += kPlanThreads) {
+      const uint64_t v = buf[i];
+      int rank = 0;
+      for (int k = 0; k < total; ++k) rank += buf[k] > v;
+      entries[rank] = v;
+    }
+  }
+  if (threadIdx.x == 0) *count = total * a.num_kv_heads;
+}
+
+// ---------------------------------------------------------------- producer
+
+// The producer is a whole warp: one TMA copy takes its issuing thread about
+// a hundred cycles, so the copies of a key tile go out from 16 lanes at once
+// (lanes 0-7: this CTA's K boxes, block lane / 2 of its 64 keys, 64-column
+// half lane % 2; lanes 8-15: V block lane - 8 of the tile, this CTA's 64
+// columns).  Each lane loads the block id of its box one tile ahead.
+__device__ __forceinline__ int lane_block_id(const int32_t* table, int j, int nkeys, int bs, int blk) {
+  return (blk >= 0 && kTile * j + blk * bs < nkeys) ? __ldg(table + kTile * j / bs + blk) : -1;
+}
+
+template <int G>
+__device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                              const CUtensorMap* qmap, const AttnArgs& a, uint8_t* smem,
+                                              const Bars& b, const uint64_t* items, int count, uint32_t rank) {
+  using L = Layout;
+  constexpr int TQ = kTile / G;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
+    prefetch_tensormap(qmap);
+    prefetch_tensormap(kmap);
+    prefetch_tensormap(vmap);
+  }
+  const bool leader = rank == 0;
+  const int bs = a.block_size;
+  const uint32_t box = static_cast<uint32_t>(bs * 128);  // bytes of one 64-column arena-block box
+  const int oob_row = a.num_blocks * a.num_kv_heads * bs;  // past the tensor: zero fill
+  const bool k_lane = lane < 8, v_lane = lane >= 8 && lane < 16;
+  const int kblk = lane >> 1, kreg = lane & 1, vblk = lane - 8;
+  const int k_first = 64 * static_cast<int>(rank) / bs;  // this CTA's first block of a key tile
+  const int my_blk = k_lane ? k_first + kblk : (v_lane ? vblk : -1);
+  int g = 0;  // key tiles issued by this CTA
+  int items_done = 0;
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int idx = item_index(r);
+    if (idx >= count) break;
+    const Item it = item_at(items, idx, a.num_kv_heads);
+    const QuadGeom p = quad_geom<G>(a, it.s, it.quad, static_cast<int>(rank));
+    if (p.ntiles == 0) {
+      if (leader && lane == 0) report(a.status, KSHIPRA_DEV_BAD_POSITION);
+      continue;
+    }
+    const int32_t* table = a.block_tables + static_cast<size_t>(it.s) * a.max_blocks_per_seq;
+    int next_id = lane_block_id(table, 0, p.nkeys, bs, my_blk);
+    if (items_done > 0 && !warp_wait(b.q_empty, (items_done - 1) & 1, a.status)) { ok = false; break; }
+    if (leader && lane == 0) mbar_arrive_expect_tx(b.q_full, 4 * L::kQTile);  // both CTAs, zero-filled rows included
+    __syncwarp();
+    if (lane < 4) {
+      const int reg = lane & 1, tb = lane >> 1;
+      tma_load_3d_pair(smem + (tb ? L::kQB : L::kQA) + reg * L::kQRegion, qmap, 64 * reg, it.h * G,
+                       p.q0 + p.tok + TQ * tb, map_to_rank(b.q_full, 0));
+    }
+    ++items_done;
+    for (int j = 0; j < p.ntiles; ++j, ++g) {
+      const int st = g & (kStages - 1), use = g / kStages;
+      const int id = next_id;
+      if (j + 1 < p.ntiles) next_id = lane_block_id(table, j + 1, p.nkeys, bs, my_blk);
+      const bool last = j + 1 == p.ntiles;
+      const int nv = ceil_div(min(kTile, p.nkeys - kTile * j), bs);
+      const int k_own = 64 * static_cast<int>(rank), k_peer = 64 - k_own;
+      const int nk_own = p.nkeys > kTile * j + k_own ? ceil_div(min(64, p.nkeys - kTile * j - k_own), bs) : 0;
+      const int nk_peer = p.nkeys > kTile * j + k_peer ? ceil_div(min(64, p.nkeys - kTile * j - k_peer), bs) : 0;
+      const bool has_k = k_lane && kblk < nk_own;
+      const bool has_v = v_lane && vblk < nv;
+      int row = oob_row;
+      if (has_k || has_v) {
+        if (id < 0 || id >= a.num_blocks)
+          report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
+        else
+          row = (id * a.num_kv_heads + it.h) * bs;
+      }
+      if (g >= kStages && !warp_wait(&b.kv_empty[st], (use - 1) & 1, a.status)) { ok = false; break; }
+      if (lane == 0) {
+        // the leader expects both CTAs' K halves and, but for the last tile,
+        // both V halves; an item's last V tile lands on each CTA's v_last,
+        // where tile A's softmax warps zero the rows past the last key before
+        // reporting P ready (which is what that tile's PV MMAs wait for)
+        const uint32_t kv_bytes = static_cast<uint32_t>(nk_own + nk_peer) * 2 * box +
+                                  (last ? 0u : static_cast<uint32_t>(2 * nv) * box);
+        if (leader) mbar_arrive_expect_tx(&b.kv_full[st], kv_bytes);
+        if (last) mbar_arrive_expect_tx(b.v_last, static_cast<uint32_t>(nv) * box);
+      }
+      __syncwarp();
+      const uint32_t kv_bar = map_to_rank(&b.kv_full[st], 0);
+      if (has_k)
+        tma_load_2d_pair(smem + L::kK + st * L::kKStage + kreg * L::kKRegion + kblk * bs * 128, kmap, 64 * kreg,
+                         row, kv_bar);
+      if (has_v) {
+        uint8_t* vdst = smem + L::kV + st * L::kVStage + vblk * bs * 128;
+        if (!last)
+          tma_load_2d_pair(vdst, vmap, 64 * static_cast<int>(rank), row, kv_bar);
+        else
+          tma_load_2d(vdst, vmap, 64 * static_cast<int>(rank), row, b.v_last);
+      }
+    }
+  }
+  if (!ok) {
+    // copies in flight complete on the leader's barriers, which this warp
+    // may not be able to observe: give them time to land (they take
+    // microseconds) before the pair tears down
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 2000000ull) {
+    }
+  }
+}
+
+// ---------------------------------------------------------------- MMA issuer
+
+// Descriptor words of the tiles the MMA issuer streams over (the low word
+// carries the start address, so stepping along a tile adds a constant).
+struct Descs {
+  uint32_t q_lo[2], k_lo, v_lo;  // stage 0 of K and V; stage st adds st x the stage size
+  uint32_t qk_hi, v_hi;
+};
+
+__device__ __forceinline__ uint32_t lo_word(uint64_t d) { return static_cast<uint32_t>(d); }
+__device__ __forceinline__ uint32_t hi_word(uint64_t d) { return static_cast<uint32_t>(d >> 32); }
+
+// S_x = Q_x K^T over both CTAs (rows: leader then peer; columns: the
+// leader's 64 keys then the peer's), then signal s_full[x] in both CTAs.
+template <bool kBf16>
+__device__ __forceinline__ void issue_qk(const Descs& dd, const Bars& b, uint32_t tmem, int x, int st) {
+  using L = Layout;
+  constexpr uint32_t kIdescQK = idesc_f16(kBf16, 2 * kTile, kTile, false, false);
+  const uint32_t q_lo = x ? dd.q_lo[1] : dd.q_lo[0];
+  const uint32_t k_lo = dd.k_lo + static_cast<uint32_t>(st) * (L::kKStage >> 4);
+#pragma unroll
+  for (int ks = 0; ks < kD / 16; ++ks) {
+    const uint32_t q_off = ((ks >> 2) * L::kQRegion + (ks & 3) * 32) >> 4;
+    const uint32_t k_off = ((ks >> 2) * L::kKRegion + (ks & 3) * 32) >> 4;
+    umma_pair_ss_w(tmem + kTile * x, q_lo + q_off, dd.qk_hi, k_lo + k_off, dd.qk_hi, kIdescQK, ks > 0 ? 1u : 0u);
+  }
+  umma_commit_pair(&b.s_full[x]);
+}
+
+// O_x (+)= P_x V.  P_x is read from TMEM over S_x: keys 16 kk.. of step kk in
+// columns 8 kk (kk < 4) or 8 kk + 32 (kk >= 4).  V is MN-major, one 64-column
+// swizzle atom per CTA (the leader's columns of O, then the peer's); 8-key
+// row groups 1024 B apart, 16 keys = 2048 B per step.
+template <bool kBf16>
+__device__ __forceinline__ void issue_pv(const Descs& dd, uint32_t tmem, int x, int st, bool accumulate) {
+  constexpr uint32_t kIdescPV = idesc_f16(kBf16, 2 * kTile, kD, false, true);
+  const uint32_t v_lo = dd.v_lo + static_cast<uint32_t>(st) * (Layout::kVStage >> 4);
+  const uint32_t acc = accumulate ? 1u : 0u;
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    umma_pair_ts_w(tmem + 2 * kTile + kTile * x, tmem + kTile * x + 8 * kk + (kk >= 4 ? 32 : 0),
+                   v_lo + ((kk * 16 * 128) >> 4), dd.v_hi, kIdescPV, kk > 0 ? 1u : acc);
+}
+
+template <bool kBf16, int G>
+__device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem,
+                                         const uint64_t* items, int count) {
+  using L = Layout;
+  const uint32_t sb = smem_u32(smem);
+  Descs dd;
+  dd.q_lo[0] = lo_word(smem_desc_sw128(sb + L::kQA, 16, 1024));
+  dd.q_lo[1] = lo_word(smem_desc_sw128(sb + L::kQB, 16, 1024));
+  dd.k_lo = lo_word(smem_desc_sw128(sb + L::kK, 16, 1024));
+  dd.v_lo = lo_word(smem_desc_sw128(sb + L::kV, L::kVStage, 1024));
+  dd.qk_hi = hi_word(smem_desc_sw128(sb, 16, 1024));
+  dd.v_hi = hi_word(smem_desc_sw128(sb, L::kVStage, 1024));
+  bool ok = true, issued_any = false;
+  int g = 0, items_done = 0;
+
+  for (int r = 0; ok; ++r) {
+    const int idx = item_index(r);
+    if (idx >= count) break;
+    const Item it = item_at(items, idx, a.num_kv_heads);
+    const QuadGeom p = quad_geom<G>(a, it.s, it.quad, 0);
+    const int n = p.ntiles;
+    if (n == 0) continue;
+    if (!mbar_wait_cluster(b.q_full, items_done & 1, a.status)) { ok = false; break; }
+    const bool wait_o = items_done > 0;  // the previous item's epilogues must have read O_A / O_B
+    const int g0 = g;
+    const int st0 = g0 & (kStages - 1);
+    if (!mbar_wait_cluster(&b.kv_full[st0], (g0 / kStages) & 1, a.status)) { ok = false; break; }
+    tc_fence_after();
+    issue_qk<kBf16>(dd, b, tmem, 0, st0);
+    issue_qk<kBf16>(dd, b, tmem, 1, st0);
+    issued_any = true;
+    if (n == 1) umma_commit_pair(b.q_empty);
+    for (int j = 0; j < n && ok; ++j) {
+      const int gt = g0 + j, st = gt & (kStages - 1);
+      // tile A: PV(j), then QK(j + 1)
+      if (!mbar_wait_cluster(&b.p_full[0], gt & 1, a.status) ||
+          (j == 0 && wait_o && !mbar_wait_cluster(&b.o_free[0], (items_done - 1) & 1, a.status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_pv<kBf16>(dd, tmem, 0, st, j > 0);
+      const int st1 = (gt + 1) & (kStages - 1);
+      if (j + 1 < n) {
+        if (!mbar_wait_cluster(&b.kv_full[st1], ((gt + 1) / kStages) & 1, a.status)) { ok = false; break; }
+        tc_fence_after();
+        issue_qk<kBf16>(dd, b, tmem, 0, st1);
+      } else {
+        umma_commit_pair(&b.o_full[0]);
+      }
+      // tile B: PV(j), then QK(j + 1)
+      if (!mbar_wait_cluster(&b.p_full[1], gt & 1, a.status) ||
+          (j == 0 && wait_o && !mbar_wait_cluster(&b.o_free[1], (items_done - 1) & 1, a.status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      issue_pv<kBf16>(dd, tmem, 1, st, j > 0);
+      umma_commit_pair(&b.kv_empty[st]);  // K(j) and V(j) have no later reader
+      if (j + 1 < n) {
+        issue_qk<kBf16>(dd, b, tmem, 1, st1);
+        if (j + 2 == n) umma_commit_pair(b.q_empty);
+      } else {
+        umma_commit_pair(&b.o_full[1]);
+      }
+    }
+    g += n;
+    ++items_done;
+  }
+  if (!ok && issued_any) {  // wait for this thread's MMAs before tensor memory is released
+    umma_commit_pair(b.drain);
+    drain_wait(b.drain, 0);
+  }
+}
+
+// ---------------------------------------------------------------- softmax
+
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+// Named barrier for the two warps that share a row range (same TMEM lanes).
+__device__ __forceinline__ void pair_sync(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+
+// One arrival per warp on a barrier of the leader CTA, after every lane's
+// tensor-memory and shared-memory writes.
+__device__ __forceinline__ void warp_arrive_leader(uint32_t bar_cluster) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(bar_cluster);
+}
+
+// Each row of tile x is handled by two threads: `half` 0 takes key columns
+// 0-63 (and O columns 0..63), half 1 the other halves.  They exchange their
+// partial row maxima every key tile and their partial sums at the end.
+template <bool kBf16, int G>
+__device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem,
+                                             const uint64_t* items, int count, int x, int half, uint32_t rank) {
+  using L = Layout;
+  constexpr int TQ = kTile / G;
+  constexpr int HC = kTile / 2;  // key columns per thread
+  constexpr int HD = kD / 2;     // O columns per thread
+  // the reference maximum of the exponents is raised only when the row
+  // maximum passes it by more than 2^8 (exp2 units): probabilities stay below
+  // 2^8, well inside fp16/bf16 range, and O / l is unchanged
+  constexpr float kRescaleThreshold = 8.f;
+  const int quarter = (threadIdx.x >> 5) & 3;
+  const int r = 32 * quarter + (threadIdx.x & 31);  // row of tile x = TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
+  const uint32_t s_tmem = tmem + kTile * x + lane_off;
+  const uint32_t o_tmem = tmem + 2 * kTile + kTile * x + lane_off + HD * half;
+  const int bar_id = 1 + 4 * x + quarter;
+  float* xmax = reinterpret_cast<float*>(smem + L::kX) + x * 2 * 2 * kTile;  // [parity][half][row]
+  float* xsum = reinterpret_cast<float*>(smem + L::kX) + 2 * 2 * 2 * kTile + x * 2 * kTile;  // [half][row]
+  const float c2 = a.scale_log2;
+  const int tl = r / G, gg = r % G;
+  int g = 0, items_done = 0;
+  bool ok = true;
+
+  for (int ri = 0; ok; ++ri) {
+    const int idx = item_index(ri);
+    if (idx >= count) break;
+    const Item it = item_at(items, idx, a.num_kv_heads);
+    const QuadGeom p = quad_geom<G>(a, it.s, it.quad, static_cast<int>(rank));
+    const int n = p.ntiles;
+    if (n == 0) continue;
+    const int nvalid = x == 0 ? p.n_a : p.n_b;
+    const bool row_valid = tl < nvalid;
+    // rows past the last token compute on whatever the tile holds, at the
+    // position of the quad's last token, and are never stored
+    const int tok = row_valid ? p.q0 + p.tok + TQ * x + tl : p.q0 + p.last;
+    const int pos = __ldg(a.positions + tok);
+    float m_ref = kNegInf, l = 0.f;
+
+    for (int j = 0; j < n; ++j) {
+      const int gt = g + j;
+      if (!warp_wait(&b.s_full[x], gt & 1, a.status)) { ok = false; break; }
+      tc_fence_after();
+      // pass 1: the half row's maximum over visible keys.  Only tiles that
+      // cross some row's position (warp-uniform test) pay for the mask.
+      const int kb0 = kTile * j + HC * half;
+      const bool diag = __any_sync(0xffffffffu, kb0 + HC - 1 > pos);
+      float m_tile;
+      {
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = kNegInf;
+#pragma unroll
+        for (int cc = 0; cc < HC / 32; ++cc) {
+          uint32_t t[32];
+          tmem_ld32(s_tmem + HC * half + 32 * cc, t);
+          if (diag) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              mx[i & 7] = fmaxf(mx[i & 7], kb0 + 32 * cc + i > pos ? kNegInf : __uint_as_float(t[i]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(t[i]));
+          }
+        }
+        m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      }
+      float* xm = xmax + (gt & 1) * 2 * kTile;
+      xm[half * kTile + r] = m_tile;
+      pair_sync(bar_id);
+      m_tile = fmaxf(m_tile, xm[(1 - half) * kTile + r]);  // both halves now hold the row maximum
+      const bool raise = m_tile != kNegInf && (m_ref == kNegInf || (m_tile - m_ref) * c2 > kRescaleThreshold);
+      float alpha = 1.f;
+      if (raise) {
+        alpha = ex2((m_ref - m_tile) * c2);  // 0 on the first visible tile
+        m_ref = m_tile;
+      }
+      const float ms = (m_ref == kNegInf ? 0.f : m_ref) * c2;
+      // pass 2, 32 keys at a time: probabilities, their sum, and P (two per
+      // column) written over this half's own, already read, S columns:
+      // keys 32 cc + [0, 32) of half h go to columns 64 h + 16 cc + [0, 16)
+      float sums[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int cc = 0; cc < HC / 32; ++cc) {
+        uint32_t t[32];
+        tmem_ld32(s_tmem + HC * half + 32 * cc, t);
+        uint32_t pk[16];
+        if (diag) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int k0 = kb0 + 32 * cc + 2 * i;
+            const float p0 = k0 > pos ? 0.f : ex2(fmaf(__uint_as_float(t[2 * i]), c2, -ms));
+            const float p1 = k0 + 1 > pos ? 0.f : ex2(fmaf(__uint_as_float(t[2 * i + 1]), c2, -ms));
+            sums[i & 3] += p0 + p1;
+            pk[i] = pack2<kBf16>(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(__uint_as_float(t[2 * i]), c2, -ms));
+            const float p1 = ex2(fmaf(__uint_as_float(t[2 * i + 1]), c2, -ms));
+            sums[i & 3] += p0 + p1;
+            pk[i] = pack2<kBf16>(p0, p1);
+          }
+        }
+        tmem_st16(s_tmem + HC * half + 16 * cc, pk);
+      }
+      l = fmaf(l, alpha, (sums[0] + sums[1]) + (sums[2] + sums[3]));
+      // PV of the previous key tile completed before S of this one (same
+      // issuing thread, committed in order), so O can be rescaled here
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t t[32];
+          tmem_ld32(o_tmem + 32 * c, t);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+          tmem_st32(o_tmem + 32 * c, t);
+        }
+      }
+      if (x == 0 && j == n - 1) {
+        // the item's last V tile lands on this CTA's v_last; value rows past
+        // the last needed key may hold anything (even NaN, or nothing loaded
+        // at all): zero them so that P = 0 contributes 0.  Tile A's "P ready"
+        // is what the leader waits for before this tile's PV MMAs.
+        if (!warp_wait(b.v_last, items_done & 1, a.status)) { ok = false; break; }
+        if (r >= p.nkeys - kTile * j) {
+          const uint32_t vrow = smem_u32(smem + L::kV + (gt & (kStages - 1)) * L::kVStage) + r * 128 + 64 * half;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) st_shared_zero16(vrow + c * 16);
+        }
+        fence_proxy_async_smem();
+      }
+      warp_arrive_leader(map_to_rank(&b.p_full[x], 0));
+    }
+    if (!ok) break;
+    g += n;
+    xsum[half * kTile + r] = l;
+    pair_sync(bar_id);
+    l += xsum[(1 - half) * kTile + r];
+    if (!warp_wait(&b.o_full[x], items_done & 1, a.status)) { ok = false; break; }
+    tc_fence_after();
+    const float inv = 1.f / l;
+    uint16_t* dst = static_cast<uint16_t*>(a.out) +
+                    (static_cast<size_t>(tok) * a.num_q_heads + it.h * G + gg) * kD + HD * half;
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) {
+      uint32_t t[32];
+      tmem_ld32(o_tmem + 32 * c, t);
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        w[i] = pack2<kBf16>(__uint_as_float(t[2 * i]) * inv, __uint_as_float(t[2 * i + 1]) * inv);
+      if (row_valid) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      }
+    }
+    warp_arrive_leader(map_to_rank(&b.o_free[x], 0));
+    pair_sync(bar_id);  // the partner has read xsum before it is written again
+    ++items_done;
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <bool kBf16, int G>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const __grid_constant__ CUtensorMap qmap, const AttnArgs a, const uint64_t* items,
+                        const int* count_ptr) {
+  using L = Layout;
+  const int count = *count_ptr;
+  if (static_cast<int>(blockIdx.x >> 1) >= count) return;  // no item for this pair (same test in both CTAs)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const Bars b = bars_at(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + L::kNumBars * 8);
+  const uint32_t rank = cluster_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(b.q_full, 1);
+    mbar_init(b.q_empty, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&b.kv_full[i], 1);
+      mbar_init(&b.kv_empty[i], 1);
+    }
+    mbar_init(b.v_last, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b.s_full[i], 1);
+      mbar_init(&b.p_full[i], 2 * 8);  // eight softmax warps per tile in each CTA
+      mbar_init(&b.o_full[i], 1);
+      mbar_init(&b.o_free[i], 2 * 8);
+    }
+    mbar_init(b.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrival or copy
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 16) {
+    softmax_role<kBf16, G>(a, smem, b, tmem, items, count, warp >> 3, (warp >> 2) & 1, rank);
+  } else if (warp == kProducerWarp) {
+    producer_role<G>(&kmap, &vmap, &qmap, a, smem, b, items, count, rank);
+  } else if (rank == 0) {
+    if (lane == 0) mma_role<kBf16, G>(a, smem, b, tmem, items, count);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal its barriers
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
+// Clusters of the persistent grid: as many pairs as fit at once (at most
+// one per two SMs), probed once per device.
+template <typename Kernel>
+int pair_clusters(Kernel* kernel, int sm_count) {
+  static std::atomic<int> cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  const int c = cached[dev & 63].load(std::memory_order_relaxed);
+  if (c > 0) return c;
+  int n = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sm_count / 2 > 0 ? sm_count / 2 : 1));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout::kAlloc;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sm_count / 2;
+  }
+  n = max(1, min(n, max(1, sm_count / 2)));
+  cached[dev & 63].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+template <bool kBf16, int G>
+cudaError_t launch_pair_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          const CUtensorMap& qmap, cudaStream_t stream) {
+  static std::atomic<unsigned long long> configured{0};
+  cudaError_t e = set_smem_limit_once(prefill_pair_kernel<kBf16, G>, Layout::kAlloc, configured);
+  if (e != cudaSuccess) return e;
+  const int clusters = pair_clusters(prefill_pair_kernel<kBf16, G>, a.sm_count);
+  prefill_pair_plan_kernel<G><<<1, kPlanThreads, 0, stream>>>(a, a.ws_items, a.ws_item_count, a.max_items);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  prefill_pair_kernel<kBf16, G><<<2 * clusters, kThreads, Layout::kAlloc, stream>>>(kmap, vmap, qmap, a,
+                                                                                   a.ws_items, a.ws_item_count);
+  return cudaGetLastError();
+}
+
+template <bool kBf16>
+cudaError_t launch_pair_g(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          const CUtensorMap& qmap, cudaStream_t stream) {
+  switch (a.group) {
+    case 1: return launch_pair_t<kBf16, 1>(a, kmap, vmap, qmap, stream);
+    case 2: return launch_pair_t<kBf16, 2>(a, kmap, vmap, qmap, stream);
+    case 4: return launch_pair_t<kBf16, 4>(a, kmap, vmap, qmap, stream);
+    case 8: return launch_pair_t<kBf16, 8>(a, kmap, vmap, qmap, stream);
+    case 16: return launch_pair_t<kBf16, 16>(a, kmap, vmap, qmap, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_pair(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                const CUtensorMap& qmap, cudaStream_t stream) {
+  if (a.head_dim != kD) return cudaErrorInvalidValue;
+  return a.dtype == KSHIPRA_DTYPE_BF16 ? launch_pair_g<true>(a, kmap, vmap, qmap, stream)
+                                       : launch_pair_g<false>(a, kmap, vmap, qmap, stream);
+}
+
+}  // namespace kshipra
