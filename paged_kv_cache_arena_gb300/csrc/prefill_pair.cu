@@ -20,19 +20,20 @@
 // this kernel on GB300; halving it per SM leaves the tensor core as the
 // limit.
 //
-// Roles (576 threads per CTA):
-//  - warp 16 (one lane): TMA producer.  Q_A / Q_B as 3-D boxes (token x head
+// Roles (320 threads per CTA):
+//  - warp 8: TMA producer, 16 lanes issuing at once.  Q_A / Q_B as 3-D boxes (token x head
 //    x 64 columns); this CTA's halves of each K/V tile as arena-block boxes
 //    through the block table, four stages.  Completion is counted on the
 //    leader's barriers, except the last V tile of an item, which completes on
 //    a barrier of its own CTA so the softmax warps can zero its tail.
-//  - warp 17 (one lane, leader only): MMA issuer, ping-pong between A and B:
+//  - warp 9 (one lane, leader only): MMA issuer, ping-pong between A and B:
 //    S_X = Q_X K^T (M 256, N 128, K 128) into TMEM, then O_X += P_X V
 //    (M 256, N 128, K 128) with P_X read from TMEM, written there over S_X by
 //    the softmax.  Commits arrive on both CTAs' barriers.
-//  - warps 0-7 / 8-15: softmax of tile A / B of their own CTA, two threads per
-//    row (one per 64-key half), exactly as in the one-CTA kernel; each warp
-//    reports "P ready" / "O read" to the leader with one remote arrival.
+//  - warps 0-3 / 4-7: softmax of tile A / B of their own CTA, one thread per
+//    row: the whole S row is read into registers once, P written back over
+//    it; each warp reports "P ready" / "O read" to the leader with one remote
+//    arrival.
 // TMEM (each CTA): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Every wait is bounded; on a timeout all roles stop and drain their own
 // outstanding copies / MMAs before the pair releases tensor memory.
@@ -46,10 +47,11 @@ namespace {
 
 constexpr int kTile = 128;  // query rows per tile and keys per key tile
 constexpr int kD = 128;
-constexpr int kThreads = 576;
-constexpr int kProducerWarp = 16;
-constexpr int kMmaWarp = 17;
+constexpr int kThreads = 320;  // 8 softmax warps, producer warp, MMA warp
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kStages = 4;  // power of two
+constexpr int kSortCapacity = 1024;  // work-list entries sorted by cost
 constexpr uint32_t kTmemCols = 512;
 constexpr float kNegInf = -INFINITY;
 
@@ -63,11 +65,13 @@ struct Layout {
   static constexpr int kQB = kQA + kQTile;
   static constexpr int kK = kQB + kQTile;
   static constexpr int kV = kK + kStages * kKStage;
-  static constexpr int kX = kV + kStages * kVStage;  // row max / sum exchange between half-row threads
-  static constexpr int kXBytes = (2 * 2 * 2 + 2 * 2) * kTile * 4;
-  static constexpr int kBar = kX + kXBytes;
-  static constexpr int kNumBars = 2 + 2 * kStages + 1 + 8 + 1;
-  static constexpr int kBytes = kBar + kNumBars * 8 + 16;
+  static constexpr int kBar = kV + kStages * kVStage;
+  static constexpr int kNumBars = 2 + 3 * kStages + 8 + 1;
+  static constexpr int kPlan = kBar + kNumBars * 8 + 16;  // work list planned in the kernel
+  static constexpr int kPlanSorted = kPlan;                 // [kSortCapacity] sorted entries
+  static constexpr int kPlanBuf = kPlanSorted + kSortCapacity * 8;  // [kSortCapacity] listed entries
+  static constexpr int kPlanWarp = kPlanBuf + kSortCapacity * 8;   // per-warp totals, running base
+  static constexpr int kBytes = kPlanWarp + 64;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
@@ -76,11 +80,12 @@ struct Bars {
   uint64_t* q_empty;  // both: the item's last QK MMAs completed
   uint64_t* kv_full;   // [kStages] leader: both CTAs' K (and V, but for an item's last tile) landed
   uint64_t* kv_empty;  // [kStages] both: the stage's last PV MMA completed
-  uint64_t* v_last;   // own CTA: the item's last V tile landed in this CTA
+  uint64_t* v_last;   // [kStages] own CTA: one phase per use of the stage; an item's
+                      // last V tile lands here (other uses complete it at once)
   uint64_t* s_full;   // [2] both
-  uint64_t* p_full;   // [2] leader, 16 warp arrivals (8 per CTA)
+  uint64_t* p_full;   // [2] leader, 8 warp arrivals (4 per CTA)
   uint64_t* o_full;   // [2] both
-  uint64_t* o_free;   // [2] leader, 16 warp arrivals
+  uint64_t* o_free;   // [2] leader, 8 warp arrivals
   uint64_t* drain;    // leader
 };
 
@@ -92,7 +97,7 @@ __device__ __forceinline__ Bars bars_at(uint8_t* smem) {
   b.kv_full = p + 2;
   b.kv_empty = b.kv_full + kStages;
   b.v_last = b.kv_empty + kStages;
-  b.s_full = b.v_last + 1;
+  b.s_full = b.v_last + kStages;
   b.p_full = b.s_full + 2;
   b.o_full = b.p_full + 2;
   b.o_free = b.o_full + 2;
@@ -171,23 +176,20 @@ __device__ __forceinline__ QuadGeom quad_geom(const AttnArgs& a, int s, int quad
 }
 
 // Lists one entry per (prefill sequence, quad) -- sequences with query_len x
-// group rows above the decode threshold -- sorts them by cost (rank sort,
-// entries are distinct) and writes them to entries[]; *count receives
-// entries x num_kv_heads.  One CTA.
-constexpr int kPlanThreads = 256;
-constexpr int kSortCapacity = 1024;  // longer lists keep plan order
+// group rows above the decode threshold -- into buf[] (unsorted), sorts them
+// by cost (rank sort, entries are distinct) into out[], and returns the
+// number of entries to every thread.  Run by one whole CTA of NT threads.
+// Lists longer than kSortCapacity keep plan order (written to out[] as they
+// are listed), which the caller allows only when out[] is in global memory.
 
-template <int G>
-__global__ void __launch_bounds__(kPlanThreads) prefill_pair_plan_kernel(const AttnArgs a, uint64_t* entries,
-                                                                          int* count, int max_entries) {
+template <int G, int NT>
+__device__ int plan_entries(const AttnArgs& a, uint64_t* buf, int* warp_total, int* base, uint64_t* out,
+                            int max_entries) {
   constexpr int TQ = kTile / G;
-  __shared__ uint64_t buf[kSortCapacity];
-  __shared__ int warp_total[kPlanThreads / 32];
-  __shared__ int base;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) base = 0;
+  if (threadIdx.x == 0) *base = 0;
   __syncthreads();
-  for (int s0 = 0; s0 < a.num_seqs; s0 += kPlanThreads) {
+  for (int s0 = 0; s0 < a.num_seqs; s0 += NT) {
     const int s = s0 + threadIdx.x;
     int quads = 0, q0 = 0, qlen = 0;
     if (s < a.num_seqs) {
@@ -204,32 +206,48 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_pair_plan_kernel(const A
     }
     if (lane == 31) warp_total[warp] = incl;
     __syncthreads();
-    int before = base;
+    int before = *base;
     for (int w = 0; w < warp; ++w) before += warp_total[w];
-    int out = before + incl - quads;
-    for (int q = 0; q < quads; ++q, ++out) {
+    int o = before + incl - quads;
+    for (int q = 0; q < quads; ++q, ++o) {
       const int last = min(qlen, 4 * TQ * (q + 1)) - 1;
       const int nkeys = __ldg(a.positions + q0 + last) + 1;
       const uint32_t cost = static_cast<uint32_t>(min(max(ceil_div(nkeys, kTile), 0), 0xFFFF));
-      if (out >= max_entries) continue;
+      if (o >= max_entries) continue;
       const uint64_t v = entry_pack(cost, s, q);
-      if (out < kSortCapacity) buf[out] = v;
-      entries[out] = v;
+      if (o < kSortCapacity) buf[o] = v;
+      else out[o] = v;
     }
     __syncthreads();
     if (threadIdx.x == 0)
-      for (int w = 0; w < kPlanThreads / 32; ++w) base += warp_total[w];
+      for (int w = 0; w < NT / 32; ++w) *base += warp_total[w];
     __syncthreads();
   }
-  const int total = min(base, max_entries);
-  if (total <= kSortCapacity) {
-    for (int i = threadIdx.x; i < total; i += kPlanThreads) {
-      const uint64_t v = buf[i];
-      int rank = 0;
+  const int total = min(*base, max_entries);
+  for (int i = threadIdx.x; i < min(total, kSortCapacity); i += NT) {
+    const uint64_t v = buf[i];
+    int rank = 0;
+    if (total <= kSortCapacity)
       for (int k = 0; k < total; ++k) rank += buf[k] > v;
-      entries[rank] = v;
-    }
+    else
+      rank = i;
+    out[rank] = v;
   }
+  __syncthreads();
+  return total;
+}
+
+// Planning on its own (lists longer than the attention kernel plans for
+// itself): one CTA, entries and *count (entries x Hkv) to global memory.
+constexpr int kPlanThreads = 256;
+
+template <int G>
+__global__ void __launch_bounds__(kPlanThreads) prefill_pair_plan_kernel(const AttnArgs a, uint64_t* entries,
+                                                                          int* count, int max_entries) {
+  __shared__ uint64_t buf[kSortCapacity];
+  __shared__ int warp_total[kPlanThreads / 32];
+  __shared__ int base;
+  const int total = plan_entries<G, kPlanThreads>(a, buf, warp_total, &base, entries, max_entries);
   if (threadIdx.x == 0) *count = total * a.num_kv_heads;
 }
 
@@ -314,7 +332,13 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
         const uint32_t kv_bytes = static_cast<uint32_t>(nk_own + nk_peer) * 2 * box +
                                   (last ? 0u : static_cast<uint32_t>(2 * nv) * box);
         if (leader) mbar_arrive_expect_tx(&b.kv_full[st], kv_bytes);
-        if (last) mbar_arrive_expect_tx(b.v_last, static_cast<uint32_t>(nv) * box);
+        // a phase of v_last[st] per use of the stage, so that the softmax
+        // waiting for an item's last tile can never see a later phase (the
+        // stage is reused only after that wait)
+        if (last)
+          mbar_arrive_expect_tx(&b.v_last[st], static_cast<uint32_t>(nv) * box);
+        else
+          mbar_arrive(&b.v_last[st]);
       }
       __syncwarp();
       const uint32_t kv_bar = map_to_rank(&b.kv_full[st], 0);
@@ -326,7 +350,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
         if (!last)
           tma_load_2d_pair(vdst, vmap, 64 * static_cast<int>(rank), row, kv_bar);
         else
-          tma_load_2d(vdst, vmap, 64 * static_cast<int>(rank), row, b.v_last);
+          tma_load_2d(vdst, vmap, 64 * static_cast<int>(rank), row, &b.v_last[st]);
       }
     }
   }
@@ -370,7 +394,7 @@ __device__ __forceinline__ void issue_qk(const Descs& dd, const Bars& b, uint32_
 }
 
 // O_x (+)= P_x V.  P_x is read from TMEM over S_x: keys 16 kk.. of step kk in
-// columns 8 kk (kk < 4) or 8 kk + 32 (kk >= 4).  V is MN-major, one 64-column
+// columns 8 kk.  V is MN-major, one 64-column
 // swizzle atom per CTA (the leader's columns of O, then the peer's); 8-key
 // row groups 1024 B apart, 16 keys = 2048 B per step.
 template <bool kBf16>
@@ -380,7 +404,7 @@ __device__ __forceinline__ void issue_pv(const Descs& dd, uint32_t tmem, int x, 
   const uint32_t acc = accumulate ? 1u : 0u;
 #pragma unroll
   for (int kk = 0; kk < kTile / 16; ++kk)
-    umma_pair_ts_w(tmem + 2 * kTile + kTile * x, tmem + kTile * x + 8 * kk + (kk >= 4 ? 32 : 0),
+    umma_pair_ts_w(tmem + 2 * kTile + kTile * x, tmem + kTile * x + 8 * kk,
                    v_lo + ((kk * 16 * 128) >> 4), dd.v_hi, kIdescPV, kk > 0 ? 1u : acc);
 }
 
@@ -465,11 +489,6 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
 
-// Named barrier for the two warps that share a row range (same TMEM lanes).
-__device__ __forceinline__ void pair_sync(int id) {
-  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
-}
-
 // One arrival per warp on a barrier of the leader CTA, after every lane's
 // tensor-memory and shared-memory writes.
 __device__ __forceinline__ void warp_arrive_leader(uint32_t bar_cluster) {
@@ -478,28 +497,64 @@ __device__ __forceinline__ void warp_arrive_leader(uint32_t bar_cluster) {
   if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(bar_cluster);
 }
 
-// Each row of tile x is handled by two threads: `half` 0 takes key columns
-// 0-63 (and O columns 0..63), half 1 the other halves.  They exchange their
-// partial row maxima every key tile and their partial sums at the end.
+// A whole S row (128 key columns) into registers: four loads in flight, one
+// wait.
+__device__ __forceinline__ void load_row(uint32_t taddr, uint32_t (&t0)[32], uint32_t (&t1)[32],
+                                         uint32_t (&t2)[32], uint32_t (&t3)[32]) {
+  tmem_ld32_async(taddr, t0);
+  tmem_ld32_async(taddr + 32, t1);
+  tmem_ld32_async(taddr + 64, t2);
+  tmem_ld32_async(taddr + 96, t3);
+  tmem_wait_ld(t0);
+  reg_fence(t1);
+  reg_fence(t2);
+  reg_fence(t3);
+}
+
+// Masked scores become -inf (exp2 gives 0); the running maximum of 32 of them.
+__device__ __forceinline__ void mask_max(uint32_t (&t)[32], int k0, int pos, bool diag, float (&mx)[8]) {
+  if (diag) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (k0 + i > pos) t[i] = __float_as_uint(kNegInf);
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(t[i]));
+}
+
+// Probabilities of 32 scores, their sum, and P (two per column) into TMEM
+// (the store is waited on by the caller).
+template <bool kBf16>
+__device__ __forceinline__ void exp_store(const uint32_t (&t)[32], float c2, float ms, float (&sums)[4],
+                                          uint32_t taddr) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float p0 = ex2(fmaf(__uint_as_float(t[2 * i]), c2, -ms));
+    const float p1 = ex2(fmaf(__uint_as_float(t[2 * i + 1]), c2, -ms));
+    sums[i & 3] += p0 + p1;
+    pk[i] = pack2<kBf16>(p0, p1);
+  }
+  tmem_st16_async(taddr, pk);
+}
+
+// Thread r of tile x owns row r (TMEM lane r): it reads its whole S row once,
+// masks, finds the row maximum, and writes P over the row's first 64 columns
+// (keys 2c, 2c+1 in column c).  The reference maximum of the exponents is
+// raised only when the row maximum passes it by more than 2^8 (exp2 units):
+// probabilities stay below 2^8, well inside fp16/bf16 range, O is rarely
+// rescaled, and O / l is unchanged.
 template <bool kBf16, int G>
 __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem,
-                                             const uint64_t* items, int count, int x, int half, uint32_t rank) {
+                                             const uint64_t* items, int count, int x, uint32_t rank) {
   using L = Layout;
   constexpr int TQ = kTile / G;
-  constexpr int HC = kTile / 2;  // key columns per thread
-  constexpr int HD = kD / 2;     // O columns per thread
-  // the reference maximum of the exponents is raised only when the row
-  // maximum passes it by more than 2^8 (exp2 units): probabilities stay below
-  // 2^8, well inside fp16/bf16 range, and O / l is unchanged
   constexpr float kRescaleThreshold = 8.f;
   const int quarter = (threadIdx.x >> 5) & 3;
   const int r = 32 * quarter + (threadIdx.x & 31);  // row of tile x = TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
   const uint32_t s_tmem = tmem + kTile * x + lane_off;
-  const uint32_t o_tmem = tmem + 2 * kTile + kTile * x + lane_off + HD * half;
-  const int bar_id = 1 + 4 * x + quarter;
-  float* xmax = reinterpret_cast<float*>(smem + L::kX) + x * 2 * 2 * kTile;  // [parity][half][row]
-  float* xsum = reinterpret_cast<float*>(smem + L::kX) + 2 * 2 * 2 * kTile + x * 2 * kTile;  // [half][row]
+  const uint32_t o_tmem = tmem + 2 * kTile + kTile * x + lane_off;
   const float c2 = a.scale_log2;
   const int tl = r / G, gg = r % G;
   int g = 0, items_done = 0;
@@ -524,34 +579,21 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
       const int gt = g + j;
       if (!warp_wait(&b.s_full[x], gt & 1, a.status)) { ok = false; break; }
       tc_fence_after();
-      // pass 1: the half row's maximum over visible keys.  Only tiles that
-      // cross some row's position (warp-uniform test) pay for the mask.
-      const int kb0 = kTile * j + HC * half;
-      const bool diag = __any_sync(0xffffffffu, kb0 + HC - 1 > pos);
-      float m_tile;
-      {
-        float mx[8];
+      uint32_t t0[32], t1[32], t2[32], t3[32];
+      load_row(s_tmem, t0, t1, t2, t3);
+      // only tiles that cross some row's position (warp-uniform test) pay
+      // for the mask
+      const int kb0 = kTile * j;
+      const bool diag = __any_sync(0xffffffffu, kb0 + kTile - 1 > pos);
+      float mx[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = kNegInf;
-#pragma unroll
-        for (int cc = 0; cc < HC / 32; ++cc) {
-          uint32_t t[32];
-          tmem_ld32(s_tmem + HC * half + 32 * cc, t);
-          if (diag) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              mx[i & 7] = fmaxf(mx[i & 7], kb0 + 32 * cc + i > pos ? kNegInf : __uint_as_float(t[i]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(t[i]));
-          }
-        }
-        m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      }
-      float* xm = xmax + (gt & 1) * 2 * kTile;
-      xm[half * kTile + r] = m_tile;
-      pair_sync(bar_id);
-      m_tile = fmaxf(m_tile, xm[(1 - half) * kTile + r]);  // both halves now hold the row maximum
+      for (int k = 0; k < 8; ++k) mx[k] = kNegInf;
+      mask_max(t0, kb0, pos, diag, mx);
+      mask_max(t1, kb0 + 32, pos, diag, mx);
+      mask_max(t2, kb0 + 64, pos, diag, mx);
+      mask_max(t3, kb0 + 96, pos, diag, mx);
+      const float m_tile =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const bool raise = m_tile != kNegInf && (m_ref == kNegInf || (m_tile - m_ref) * c2 > kRescaleThreshold);
       float alpha = 1.f;
       if (raise) {
@@ -559,41 +601,18 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
         m_ref = m_tile;
       }
       const float ms = (m_ref == kNegInf ? 0.f : m_ref) * c2;
-      // pass 2, 32 keys at a time: probabilities, their sum, and P (two per
-      // column) written over this half's own, already read, S columns:
-      // keys 32 cc + [0, 32) of half h go to columns 64 h + 16 cc + [0, 16)
       float sums[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int cc = 0; cc < HC / 32; ++cc) {
-        uint32_t t[32];
-        tmem_ld32(s_tmem + HC * half + 32 * cc, t);
-        uint32_t pk[16];
-        if (diag) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int k0 = kb0 + 32 * cc + 2 * i;
-            const float p0 = k0 > pos ? 0.f : ex2(fmaf(__uint_as_float(t[2 * i]), c2, -ms));
-            const float p1 = k0 + 1 > pos ? 0.f : ex2(fmaf(__uint_as_float(t[2 * i + 1]), c2, -ms));
-            sums[i & 3] += p0 + p1;
-            pk[i] = pack2<kBf16>(p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(__uint_as_float(t[2 * i]), c2, -ms));
-            const float p1 = ex2(fmaf(__uint_as_float(t[2 * i + 1]), c2, -ms));
-            sums[i & 3] += p0 + p1;
-            pk[i] = pack2<kBf16>(p0, p1);
-          }
-        }
-        tmem_st16(s_tmem + HC * half + 16 * cc, pk);
-      }
+      exp_store<kBf16>(t0, c2, ms, sums, s_tmem);
+      exp_store<kBf16>(t1, c2, ms, sums, s_tmem + 16);
+      exp_store<kBf16>(t2, c2, ms, sums, s_tmem + 32);
+      exp_store<kBf16>(t3, c2, ms, sums, s_tmem + 48);
+      tmem_wait_st();
       l = fmaf(l, alpha, (sums[0] + sums[1]) + (sums[2] + sums[3]));
       // PV of the previous key tile completed before S of this one (same
       // issuing thread, committed in order), so O can be rescaled here
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < kD / 32; ++c) {
           uint32_t t[32];
           tmem_ld32(o_tmem + 32 * c, t);
 #pragma unroll
@@ -606,11 +625,12 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
         // the last needed key may hold anything (even NaN, or nothing loaded
         // at all): zero them so that P = 0 contributes 0.  Tile A's "P ready"
         // is what the leader waits for before this tile's PV MMAs.
-        if (!warp_wait(b.v_last, items_done & 1, a.status)) { ok = false; break; }
+        const int st = gt & (kStages - 1);
+        if (!warp_wait(&b.v_last[st], (gt / kStages) & 1, a.status)) { ok = false; break; }
         if (r >= p.nkeys - kTile * j) {
-          const uint32_t vrow = smem_u32(smem + L::kV + (gt & (kStages - 1)) * L::kVStage) + r * 128 + 64 * half;
+          const uint32_t vrow = smem_u32(smem + L::kV + st * L::kVStage) + r * 128;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) st_shared_zero16(vrow + c * 16);
+          for (int c = 0; c < 8; ++c) st_shared_zero16(vrow + c * 16);
         }
         fence_proxy_async_smem();
       }
@@ -618,16 +638,13 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
     }
     if (!ok) break;
     g += n;
-    xsum[half * kTile + r] = l;
-    pair_sync(bar_id);
-    l += xsum[(1 - half) * kTile + r];
     if (!warp_wait(&b.o_full[x], items_done & 1, a.status)) { ok = false; break; }
     tc_fence_after();
     const float inv = 1.f / l;
-    uint16_t* dst = static_cast<uint16_t*>(a.out) +
-                    (static_cast<size_t>(tok) * a.num_q_heads + it.h * G + gg) * kD + HD * half;
+    uint16_t* dst =
+        static_cast<uint16_t*>(a.out) + (static_cast<size_t>(tok) * a.num_q_heads + it.h * G + gg) * kD;
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) {
+    for (int c = 0; c < kD / 32; ++c) {
       uint32_t t[32];
       tmem_ld32(o_tmem + 32 * c, t);
       uint32_t w[16];
@@ -641,7 +658,6 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
       }
     }
     warp_arrive_leader(map_to_rank(&b.o_free[x], 0));
-    pair_sync(bar_id);  // the partner has read xsum before it is written again
     ++items_done;
   }
 }
@@ -651,13 +667,26 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
 template <bool kBf16, int G>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                        const __grid_constant__ CUtensorMap qmap, const AttnArgs a, const uint64_t* items,
-                        const int* count_ptr) {
+                        const __grid_constant__ CUtensorMap qmap, const AttnArgs a, const uint64_t* planned,
+                        const int* planned_count, int plan_here) {
   using L = Layout;
-  const int count = *count_ptr;
-  if (static_cast<int>(blockIdx.x >> 1) >= count) return;  // no item for this pair (same test in both CTAs)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // the work list: planned here, in shared memory, when it is short enough
+  // (saves a launch), else by the planning kernel
+  const uint64_t* items = planned;
+  int count;
+  if (plan_here) {
+    uint64_t* sorted = reinterpret_cast<uint64_t*>(smem + L::kPlanSorted);
+    int* warp_total = reinterpret_cast<int*>(smem + L::kPlanWarp);
+    const int total = plan_entries<G, kThreads>(a, reinterpret_cast<uint64_t*>(smem + L::kPlanBuf), warp_total,
+                                                warp_total + 12, sorted, kSortCapacity);
+    count = total * a.num_kv_heads;
+    items = sorted;
+  } else {
+    count = *planned_count;
+  }
+  if (static_cast<int>(blockIdx.x >> 1) >= count) return;  // no item for this pair (same test in both CTAs)
   const Bars b = bars_at(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + L::kNumBars * 8);
   const uint32_t rank = cluster_rank();
@@ -669,13 +698,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&b.kv_full[i], 1);
       mbar_init(&b.kv_empty[i], 1);
+      mbar_init(&b.v_last[i], 1);
     }
-    mbar_init(b.v_last, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&b.s_full[i], 1);
-      mbar_init(&b.p_full[i], 2 * 8);  // eight softmax warps per tile in each CTA
+      mbar_init(&b.p_full[i], 2 * 4);  // four softmax warps per tile in each CTA
       mbar_init(&b.o_full[i], 1);
-      mbar_init(&b.o_free[i], 2 * 8);
+      mbar_init(&b.o_free[i], 2 * 4);
     }
     mbar_init(b.drain, 1);
     fence_mbar_init();
@@ -690,8 +719,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 16) {
-    softmax_role<kBf16, G>(a, smem, b, tmem, items, count, warp >> 3, (warp >> 2) & 1, rank);
+  if (warp < 8) {
+    softmax_role<kBf16, G>(a, smem, b, tmem, items, count, warp >> 2, rank);
   } else if (warp == kProducerWarp) {
     producer_role<G>(&kmap, &vmap, &qmap, a, smem, b, items, count, rank);
   } else if (rank == 0) {
@@ -736,10 +765,13 @@ cudaError_t launch_pair_t(const AttnArgs& a, const CUtensorMap& kmap, const CUte
   cudaError_t e = set_smem_limit_once(prefill_pair_kernel<kBf16, G>, Layout::kAlloc, configured);
   if (e != cudaSuccess) return e;
   const int clusters = pair_clusters(prefill_pair_kernel<kBf16, G>, a.sm_count);
-  prefill_pair_plan_kernel<G><<<1, kPlanThreads, 0, stream>>>(a, a.ws_items, a.ws_item_count, a.max_items);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  prefill_pair_kernel<kBf16, G><<<2 * clusters, kThreads, Layout::kAlloc, stream>>>(kmap, vmap, qmap, a,
-                                                                                   a.ws_items, a.ws_item_count);
+  const bool plan_here = a.max_items <= kSortCapacity;  // an upper bound on the entries
+  if (!plan_here) {
+    prefill_pair_plan_kernel<G><<<1, kPlanThreads, 0, stream>>>(a, a.ws_items, a.ws_item_count, a.max_items);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  prefill_pair_kernel<kBf16, G><<<2 * clusters, kThreads, Layout::kAlloc, stream>>>(
+      kmap, vmap, qmap, a, a.ws_items, a.ws_item_count, plan_here ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -41,6 +41,8 @@ CASES = {
     "d64-bf16": lambda: custom(27, Hq=16, Hkv=4, d=64, dtype="bf16", prefix=[129], qlen=[255]),
     "shared-prefix": lambda: custom(28, Hq=8, Hkv=2, prefix=[64, 96, 200], qlen=[40, 1, 70], shared_len=64,
                                     shared=(0, 1, 2)),
+    # head_dim 128 with two q heads per kv head: quads of 256 tokens on CTA pairs
+    "g2-d128": lambda: custom(35, Hq=8, Hkv=4, prefix=[300, 0, 77], qlen=[260, 513, 31]),
 }
 
 
@@ -120,3 +122,14 @@ def test_full_mixed_step_sampled(clean_status):
     dec_tokens = rng.choice(np.arange(int(w.query_start_loc[8]), w.num_tokens), 40, replace=False)
     toks = np.sort(np.concatenate([chunk_tokens, dec_tokens])).astype(np.int32)
     assert_close(got[toks], oracle.workload_attention(w, tokens=toks), w.dtype, "mixed sample")
+
+
+def test_long_work_list_planned_on_its_own(clean_status):
+    # 1030 short chunks: more work-list entries than the attention kernel
+    # plans for itself, so the planning kernel lists them (past its sort
+    # capacity in plan order); every row must still be computed once
+    S = 1030
+    prefix = [(7 * k) % 23 for k in range(S)]
+    w = custom(36, Hq=8, Hkv=2, prefix=prefix, qlen=[5] * S)
+    dw = run(w)
+    assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype, "1030 chunks")
