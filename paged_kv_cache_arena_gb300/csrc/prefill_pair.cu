@@ -20,20 +20,24 @@
 // this kernel on GB300; halving it per SM leaves the tensor core as the
 // limit.
 //
-// Roles (320 threads per CTA):
-//  - warp 8: TMA producer, 16 lanes issuing at once.  Q_A / Q_B as 3-D boxes (token x head
-//    x 64 columns); this CTA's halves of each K/V tile as arena-block boxes
-//    through the block table, four stages.  Completion is counted on the
-//    leader's barriers, except the last V tile of an item, which completes on
-//    a barrier of its own CTA so the softmax warps can zero its tail.
-//  - warp 9 (one lane, leader only): MMA issuer, ping-pong between A and B:
-//    S_X = Q_X K^T (M 256, N 128, K 128) into TMEM, then O_X += P_X V
-//    (M 256, N 128, K 128) with P_X read from TMEM, written there over S_X by
-//    the softmax.  Commits arrive on both CTAs' barriers.
+// Roles (352 threads per CTA):
+//  - warp 8: TMA producer, 16 lanes issuing at once.  Q_A / Q_B as 3-D boxes
+//    (token x head x 64 columns); this CTA's halves of each K/V tile as
+//    arena-block boxes through the block table, three stages.  Completion is
+//    counted on the leader's barriers, except the last V tile of an item,
+//    which completes on a barrier of its own CTA so the softmax warps can
+//    zero its tail.
+//  - warps 9 / 10 (one lane each, leader only): MMA issuers of tiles A / B.
+//    S_X = Q_X K^T (M 256, N 128, K 128) into TMEM; O_X += P_X V (M 256,
+//    N 128, K 128) with P_X from shared memory.  The next key tile's S_X is
+//    issued as soon as the softmax has read the current one, so scores and
+//    softmax overlap within a tile; with an issuer per tile neither tile's
+//    pipeline waits on the other's softmax.  Commits arrive on both CTAs'
+//    barriers.
 //  - warps 0-3 / 4-7: softmax of tile A / B of their own CTA, one thread per
-//    row: the whole S row is read into registers once, P written back over
-//    it; each warp reports "P ready" / "O read" to the leader with one remote
-//    arrival.
+//    row: the whole S row is read into registers once; P goes to shared
+//    memory in the MMA's operand layout; each warp reports "S read", "P
+//    ready" and "O read" to the leader with one remote arrival.
 // TMEM (each CTA): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Every wait is bounded; on a timeout all roles stop and drain their own
 // outstanding copies / MMAs before the pair releases tensor memory.
@@ -47,11 +51,11 @@ namespace {
 
 constexpr int kTile = 128;  // query rows per tile and keys per key tile
 constexpr int kD = 128;
-constexpr int kThreads = 320;  // 8 softmax warps, producer warp, MMA warp
+constexpr int kThreads = 352;  // 8 softmax warps, producer warp, two MMA warps
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kStages = 4;  // power of two
-constexpr int kSortCapacity = 1024;  // work-list entries sorted by cost
+constexpr int kMmaWarp = 9;  // and 10: the issuers of tiles A and B (leader); warp 9 also holds TMEM
+constexpr int kStages = 3;           // K/V stages
+constexpr int kSortCapacity = 128;   // work-list entries the kernel plans for itself
 constexpr uint32_t kTmemCols = 512;
 constexpr float kNegInf = -INFINITY;
 
@@ -61,32 +65,42 @@ struct Layout {
   static constexpr int kKRegion = 64 * 128;     // this CTA's 64 keys x 64 columns
   static constexpr int kKStage = 2 * kKRegion;  // 16 KB
   static constexpr int kVStage = kTile * 128;   // 128 keys x this CTA's 64 columns, 16 KB
+  static constexpr int kPTile = 2 * kQRegion;   // P: 128 rows x 128 keys, K-major, 128-byte swizzle
   static constexpr int kQA = 0;
   static constexpr int kQB = kQA + kQTile;
-  static constexpr int kK = kQB + kQTile;
+  static constexpr int kPA = kQB + kQTile;
+  static constexpr int kPB = kPA + kPTile;
+  static constexpr int kK = kPB + kPTile;
   static constexpr int kV = kK + kStages * kKStage;
   static constexpr int kBar = kV + kStages * kVStage;
-  static constexpr int kNumBars = 2 + 3 * kStages + 8 + 1;
+  static constexpr int kNumBars = 2 + 4 * kStages + 12 + 2;
   static constexpr int kPlan = kBar + kNumBars * 8 + 16;  // work list planned in the kernel
   static constexpr int kPlanSorted = kPlan;                 // [kSortCapacity] sorted entries
   static constexpr int kPlanBuf = kPlanSorted + kSortCapacity * 8;  // [kSortCapacity] listed entries
   static constexpr int kPlanWarp = kPlanBuf + kSortCapacity * 8;   // per-warp totals, running base
   static constexpr int kBytes = kPlanWarp + 64;
-  static constexpr int kAlloc = kBytes + 1024;
+  // the dynamic shared memory of a kernel without static shared variables
+  // starts at the base of the CTA's window (1024-aligned, checked at run time)
+  static constexpr int kAlloc = kBytes;
 };
+static_assert(Layout::kAlloc <= 227 * 1024, "shared memory");
 
 struct Bars {
-  uint64_t* q_full;   // leader: both CTAs' Q tiles landed
-  uint64_t* q_empty;  // both: the item's last QK MMAs completed
+  uint64_t* q_full;    // leader: both CTAs' Q tiles landed
+  uint64_t* q_empty;   // both: the item's last QK MMAs completed (one arrival per issuer)
   uint64_t* kv_full;   // [kStages] leader: both CTAs' K (and V, but for an item's last tile) landed
-  uint64_t* kv_empty;  // [kStages] both: the stage's last PV MMA completed
-  uint64_t* v_last;   // [kStages] own CTA: one phase per use of the stage; an item's
-                      // last V tile lands here (other uses complete it at once)
-  uint64_t* s_full;   // [2] both
-  uint64_t* p_full;   // [2] leader, 8 warp arrivals (4 per CTA)
-  uint64_t* o_full;   // [2] both
-  uint64_t* o_free;   // [2] leader, 8 warp arrivals
-  uint64_t* drain;    // leader
+  uint64_t* kv_empty;  // [kStages] both: the stage's PV MMAs completed (one arrival per issuer)
+  uint64_t* v_last;    // [kStages] own CTA: one phase per use of the stage; an item's
+                       // last V tile lands here (other uses complete it at once)
+  uint64_t* v_zeroed;  // [kStages] leader, 8 warp arrivals (tile A's softmax warps) per use of
+                       // the stage: the V rows past an item's last key are zeroed in both CTAs
+  uint64_t* s_full;    // [2] both: S_x ready in TMEM
+  uint64_t* s_free;    // [2] leader, 8 warp arrivals (4 per CTA): S_x read, its columns free
+  uint64_t* p_full;    // [2] leader, 8 warp arrivals: P_x written to shared memory
+  uint64_t* p_free;    // [2] both: the PV MMAs reading P_x (and accumulating O_x) completed
+  uint64_t* o_full;    // [2] both: O_x complete for the item
+  uint64_t* o_free;    // [2] leader, 8 warp arrivals: O_x read by the epilogue
+  uint64_t* drain;     // [2] leader: per issuer
 };
 
 __device__ __forceinline__ Bars bars_at(uint8_t* smem) {
@@ -97,9 +111,12 @@ __device__ __forceinline__ Bars bars_at(uint8_t* smem) {
   b.kv_full = p + 2;
   b.kv_empty = b.kv_full + kStages;
   b.v_last = b.kv_empty + kStages;
-  b.s_full = b.v_last + kStages;
-  b.p_full = b.s_full + 2;
-  b.o_full = b.p_full + 2;
+  b.v_zeroed = b.v_last + kStages;
+  b.s_full = b.v_zeroed + kStages;
+  b.s_free = b.s_full + 2;
+  b.p_full = b.s_free + 2;
+  b.p_free = b.p_full + 2;
+  b.o_full = b.p_free + 2;
   b.o_free = b.o_full + 2;
   b.drain = b.o_free + 2;
   return b;
@@ -306,7 +323,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
     }
     ++items_done;
     for (int j = 0; j < p.ntiles; ++j, ++g) {
-      const int st = g & (kStages - 1), use = g / kStages;
+      const int st = g % kStages, use = g / kStages;
       const int id = next_id;
       if (j + 1 < p.ntiles) next_id = lane_block_id(table, j + 1, p.nkeys, bs, my_blk);
       const bool last = j + 1 == p.ntiles;
@@ -369,7 +386,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
 // Descriptor words of the tiles the MMA issuer streams over (the low word
 // carries the start address, so stepping along a tile adds a constant).
 struct Descs {
-  uint32_t q_lo[2], k_lo, v_lo;  // stage 0 of K and V; stage st adds st x the stage size
+  uint32_t q_lo[2], p_lo[2], k_lo, v_lo;  // K and V: stage 0; stage st adds st x the stage size
   uint32_t qk_hi, v_hi;
 };
 
@@ -393,29 +410,43 @@ __device__ __forceinline__ void issue_qk(const Descs& dd, const Bars& b, uint32_
   umma_commit_pair(&b.s_full[x]);
 }
 
-// O_x (+)= P_x V.  P_x is read from TMEM over S_x: keys 16 kk.. of step kk in
-// columns 8 kk.  V is MN-major, one 64-column
-// swizzle atom per CTA (the leader's columns of O, then the peer's); 8-key
-// row groups 1024 B apart, 16 keys = 2048 B per step.
+// O_x (+)= P_x V.  P_x is K-major in shared memory like Q (keys 64 g .. in
+// 64-key region g); V is MN-major, one 64-column swizzle atom per CTA (the
+// leader's columns of O, then the peer's), 8-key row groups 1024 B apart,
+// 16 keys = 2048 B per step.  Then signal p_free[x] in both CTAs.
 template <bool kBf16>
-__device__ __forceinline__ void issue_pv(const Descs& dd, uint32_t tmem, int x, int st, bool accumulate) {
+__device__ __forceinline__ void issue_pv(const Descs& dd, const Bars& b, uint32_t tmem, int x, int st,
+                                         bool accumulate) {
+  using L = Layout;
   constexpr uint32_t kIdescPV = idesc_f16(kBf16, 2 * kTile, kD, false, true);
-  const uint32_t v_lo = dd.v_lo + static_cast<uint32_t>(st) * (Layout::kVStage >> 4);
+  const uint32_t p_lo = x ? dd.p_lo[1] : dd.p_lo[0];
+  const uint32_t v_lo = dd.v_lo + static_cast<uint32_t>(st) * (L::kVStage >> 4);
   const uint32_t acc = accumulate ? 1u : 0u;
 #pragma unroll
-  for (int kk = 0; kk < kTile / 16; ++kk)
-    umma_pair_ts_w(tmem + 2 * kTile + kTile * x, tmem + kTile * x + 8 * kk,
-                   v_lo + ((kk * 16 * 128) >> 4), dd.v_hi, kIdescPV, kk > 0 ? 1u : acc);
+  for (int kk = 0; kk < kTile / 16; ++kk) {
+    const uint32_t p_off = ((kk >> 2) * L::kQRegion + (kk & 3) * 32) >> 4;
+    umma_pair_ss_w(tmem + 2 * kTile + kTile * x, p_lo + p_off, dd.qk_hi, v_lo + ((kk * 16 * 128) >> 4), dd.v_hi,
+                   kIdescPV, kk > 0 ? 1u : acc);
+  }
+  umma_commit_pair(&b.p_free[x]);
 }
 
+// The MMAs of query tile x (one issuing thread per tile, so that neither
+// tile's pipeline waits on the other's softmax): per key tile j of an item,
+// S_x(j + 1) = Q_x K(j + 1)^T as soon as the softmax has read S_x(j) (the
+// next scores are computed while the softmax of this tile runs), then
+// O_x += P_x(j) V(j) once P_x(j) is in shared memory.  Barriers that cover
+// both tiles (stage empty, Q empty) count one arrival from each issuer.
 template <bool kBf16, int G>
 __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem,
-                                         const uint64_t* items, int count) {
+                                         const uint64_t* items, int count, int x) {
   using L = Layout;
   const uint32_t sb = smem_u32(smem);
   Descs dd;
   dd.q_lo[0] = lo_word(smem_desc_sw128(sb + L::kQA, 16, 1024));
   dd.q_lo[1] = lo_word(smem_desc_sw128(sb + L::kQB, 16, 1024));
+  dd.p_lo[0] = lo_word(smem_desc_sw128(sb + L::kPA, 16, 1024));
+  dd.p_lo[1] = lo_word(smem_desc_sw128(sb + L::kPB, 16, 1024));
   dd.k_lo = lo_word(smem_desc_sw128(sb + L::kK, 16, 1024));
   dd.v_lo = lo_word(smem_desc_sw128(sb + L::kV, L::kVStage, 1024));
   dd.qk_hi = hi_word(smem_desc_sw128(sb, 16, 1024));
@@ -431,55 +462,49 @@ __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const
     const int n = p.ntiles;
     if (n == 0) continue;
     if (!mbar_wait_cluster(b.q_full, items_done & 1, a.status)) { ok = false; break; }
-    const bool wait_o = items_done > 0;  // the previous item's epilogues must have read O_A / O_B
     const int g0 = g;
-    const int st0 = g0 & (kStages - 1);
-    if (!mbar_wait_cluster(&b.kv_full[st0], (g0 / kStages) & 1, a.status)) { ok = false; break; }
+    // the item's first scores, once the previous tile's S columns are read
+    if (!mbar_wait_cluster(&b.kv_full[g0 % kStages], (g0 / kStages) & 1, a.status) ||
+        (g0 > 0 && !mbar_wait_cluster(&b.s_free[x], (g0 - 1) & 1, a.status))) {
+      ok = false;
+      break;
+    }
     tc_fence_after();
-    issue_qk<kBf16>(dd, b, tmem, 0, st0);
-    issue_qk<kBf16>(dd, b, tmem, 1, st0);
+    issue_qk<kBf16>(dd, b, tmem, x, g0 % kStages);
     issued_any = true;
     if (n == 1) umma_commit_pair(b.q_empty);
-    for (int j = 0; j < n && ok; ++j) {
-      const int gt = g0 + j, st = gt & (kStages - 1);
-      // tile A: PV(j), then QK(j + 1)
-      if (!mbar_wait_cluster(&b.p_full[0], gt & 1, a.status) ||
-          (j == 0 && wait_o && !mbar_wait_cluster(&b.o_free[0], (items_done - 1) & 1, a.status))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      issue_pv<kBf16>(dd, tmem, 0, st, j > 0);
-      const int st1 = (gt + 1) & (kStages - 1);
+    for (int j = 0; j < n; ++j) {
+      const int gt = g0 + j, st = gt % kStages, st1 = (gt + 1) % kStages;
       if (j + 1 < n) {
-        if (!mbar_wait_cluster(&b.kv_full[st1], ((gt + 1) / kStages) & 1, a.status)) { ok = false; break; }
+        if (!mbar_wait_cluster(&b.s_free[x], gt & 1, a.status) ||
+            !mbar_wait_cluster(&b.kv_full[st1], ((gt + 1) / kStages) & 1, a.status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        issue_qk<kBf16>(dd, b, tmem, 0, st1);
-      } else {
-        umma_commit_pair(&b.o_full[0]);
+        issue_qk<kBf16>(dd, b, tmem, x, st1);
+        if (j + 2 == n) umma_commit_pair(b.q_empty);
       }
-      // tile B: PV(j), then QK(j + 1)
-      if (!mbar_wait_cluster(&b.p_full[1], gt & 1, a.status) ||
-          (j == 0 && wait_o && !mbar_wait_cluster(&b.o_free[1], (items_done - 1) & 1, a.status))) {
+      // the previous item's epilogue must have read O_x before PV overwrites it
+      // (tile B's last PV also waits for tile A's warps to have zeroed the V
+      // rows past the item's last key, which both tiles read)
+      if (!mbar_wait_cluster(&b.p_full[x], gt & 1, a.status) ||
+          (x == 1 && j + 1 == n && !mbar_wait_cluster(&b.v_zeroed[st], (gt / kStages) & 1, a.status)) ||
+          (j == 0 && items_done > 0 && !mbar_wait_cluster(&b.o_free[x], (items_done - 1) & 1, a.status))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      issue_pv<kBf16>(dd, tmem, 1, st, j > 0);
-      umma_commit_pair(&b.kv_empty[st]);  // K(j) and V(j) have no later reader
-      if (j + 1 < n) {
-        issue_qk<kBf16>(dd, b, tmem, 1, st1);
-        if (j + 2 == n) umma_commit_pair(b.q_empty);
-      } else {
-        umma_commit_pair(&b.o_full[1]);
-      }
+      issue_pv<kBf16>(dd, b, tmem, x, st, j > 0);
+      umma_commit_pair(&b.kv_empty[st]);  // this tile's last use of K(j), V(j)
+      if (j + 1 == n) umma_commit_pair(&b.o_full[x]);
     }
     g += n;
     ++items_done;
   }
   if (!ok && issued_any) {  // wait for this thread's MMAs before tensor memory is released
-    umma_commit_pair(b.drain);
-    drain_wait(b.drain, 0);
+    umma_commit_pair(&b.drain[x]);
+    drain_wait(&b.drain[x], 0);
   }
 }
 
@@ -522,11 +547,13 @@ __device__ __forceinline__ void mask_max(uint32_t (&t)[32], int k0, int pos, boo
   for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(t[i]));
 }
 
-// Probabilities of 32 scores, their sum, and P (two per column) into TMEM
-// (the store is waited on by the caller).
+// Probabilities of 32 scores (keys 32 cc ..), their sum, and P into row r of
+// the P tile in shared memory: K-major, 128-byte swizzle (16-byte chunk c of
+// a 128-byte row segment stored at chunk c ^ (r % 8)), keys 64 g .. in
+// region g -- the layout TMA gives Q, which the MMA reads the same way.
 template <bool kBf16>
 __device__ __forceinline__ void exp_store(const uint32_t (&t)[32], float c2, float ms, float (&sums)[4],
-                                          uint32_t taddr) {
+                                          uint32_t p_row, int cc, int r) {
   uint32_t pk[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -535,12 +562,20 @@ __device__ __forceinline__ void exp_store(const uint32_t (&t)[32], float c2, flo
     sums[i & 3] += p0 + p1;
     pk[i] = pack2<kBf16>(p0, p1);
   }
-  tmem_st16_async(taddr, pk);
+  const uint32_t seg = p_row + (cc >> 1) * Layout::kQRegion;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t c = static_cast<uint32_t>((cc & 1) * 4 + q);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(seg + ((c ^ (r & 7)) << 4)), "r"(pk[4 * q]),
+                 "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+                 : "memory");
+  }
 }
 
-// Thread r of tile x owns row r (TMEM lane r): it reads its whole S row once,
-// masks, finds the row maximum, and writes P over the row's first 64 columns
-// (keys 2c, 2c+1 in column c).  The reference maximum of the exponents is
+// Thread r of tile x owns row r (TMEM lane r): it reads its whole S row once
+// (releasing the S columns to the next QK MMAs at once), masks, finds the row
+// maximum, and writes P to row r of its P tile in shared memory.  The
+// reference maximum of the exponents is
 // raised only when the row maximum passes it by more than 2^8 (exp2 units):
 // probabilities stay below 2^8, well inside fp16/bf16 range, O is rarely
 // rescaled, and O / l is unchanged.
@@ -555,6 +590,7 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
   const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
   const uint32_t s_tmem = tmem + kTile * x + lane_off;
   const uint32_t o_tmem = tmem + 2 * kTile + kTile * x + lane_off;
+  const uint32_t p_row = smem_u32(smem + (x ? L::kPB : L::kPA)) + r * 128;
   const float c2 = a.scale_log2;
   const int tl = r / G, gg = r % G;
   int g = 0, items_done = 0;
@@ -581,6 +617,7 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
       tc_fence_after();
       uint32_t t0[32], t1[32], t2[32], t3[32];
       load_row(s_tmem, t0, t1, t2, t3);
+      warp_arrive_leader(map_to_rank(&b.s_free[x], 0));  // the next scores may overwrite S_x
       // only tiles that cross some row's position (warp-uniform test) pay
       // for the mask
       const int kb0 = kTile * j;
@@ -601,16 +638,17 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
         m_ref = m_tile;
       }
       const float ms = (m_ref == kNegInf ? 0.f : m_ref) * c2;
+      // the previous tile's PV MMAs must be done with P_x (and with O_x,
+      // which may be rescaled below) before either is written
+      if (gt > 0 && !warp_wait(&b.p_free[x], (gt - 1) & 1, a.status)) { ok = false; break; }
       float sums[4] = {0.f, 0.f, 0.f, 0.f};
-      exp_store<kBf16>(t0, c2, ms, sums, s_tmem);
-      exp_store<kBf16>(t1, c2, ms, sums, s_tmem + 16);
-      exp_store<kBf16>(t2, c2, ms, sums, s_tmem + 32);
-      exp_store<kBf16>(t3, c2, ms, sums, s_tmem + 48);
-      tmem_wait_st();
+      exp_store<kBf16>(t0, c2, ms, sums, p_row, 0, r);
+      exp_store<kBf16>(t1, c2, ms, sums, p_row, 1, r);
+      exp_store<kBf16>(t2, c2, ms, sums, p_row, 2, r);
+      exp_store<kBf16>(t3, c2, ms, sums, p_row, 3, r);
       l = fmaf(l, alpha, (sums[0] + sums[1]) + (sums[2] + sums[3]));
-      // PV of the previous key tile completed before S of this one (same
-      // issuing thread, committed in order), so O can be rescaled here
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < kD / 32; ++c) {
           uint32_t t[32];
@@ -623,18 +661,19 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
       if (x == 0 && j == n - 1) {
         // the item's last V tile lands on this CTA's v_last; value rows past
         // the last needed key may hold anything (even NaN, or nothing loaded
-        // at all): zero them so that P = 0 contributes 0.  Tile A's "P ready"
-        // is what the leader waits for before this tile's PV MMAs.
-        const int st = gt & (kStages - 1);
+        // at all): zero them so that P = 0 contributes 0.  The PV MMAs of
+        // both tiles wait for tile A's warps ("P ready" / "V zeroed").
+        const int st = gt % kStages;
         if (!warp_wait(&b.v_last[st], (gt / kStages) & 1, a.status)) { ok = false; break; }
         if (r >= p.nkeys - kTile * j) {
           const uint32_t vrow = smem_u32(smem + L::kV + st * L::kVStage) + r * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) st_shared_zero16(vrow + c * 16);
         }
-        fence_proxy_async_smem();
       }
+      fence_proxy_async_smem();  // P (and zeroed V rows) visible to the tensor cores
       warp_arrive_leader(map_to_rank(&b.p_full[x], 0));
+      if (x == 0) warp_arrive_leader(map_to_rank(&b.v_zeroed[gt % kStages], 0));
     }
     if (!ok) break;
     g += n;
@@ -670,8 +709,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap qmap, const AttnArgs a, const uint64_t* planned,
                         const int* planned_count, int plan_here) {
   using L = Layout;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled layouts need 1024-byte alignment
+    if (threadIdx.x == 0) report(a.status, KSHIPRA_DEV_TIMEOUT);
+    return;
+  }
   // the work list: planned here, in shared memory, when it is short enough
   // (saves a launch), else by the planning kernel
   const uint64_t* items = planned;
@@ -694,19 +737,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(b.q_full, 1);
-    mbar_init(b.q_empty, 1);
+    mbar_init(b.q_empty, 2);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&b.kv_full[i], 1);
-      mbar_init(&b.kv_empty[i], 1);
+      mbar_init(&b.kv_empty[i], 2);
       mbar_init(&b.v_last[i], 1);
+      mbar_init(&b.v_zeroed[i], 2 * 4);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&b.s_full[i], 1);
-      mbar_init(&b.p_full[i], 2 * 4);  // four softmax warps per tile in each CTA
+      mbar_init(&b.s_free[i], 2 * 4);  // four softmax warps per tile in each CTA
+      mbar_init(&b.p_full[i], 2 * 4);
+      mbar_init(&b.p_free[i], 1);
       mbar_init(&b.o_full[i], 1);
       mbar_init(&b.o_free[i], 2 * 4);
     }
-    mbar_init(b.drain, 1);
+    mbar_init(&b.drain[0], 1);
+    mbar_init(&b.drain[1], 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -724,7 +771,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kProducerWarp) {
     producer_role<G>(&kmap, &vmap, &qmap, a, smem, b, items, count, rank);
   } else if (rank == 0) {
-    if (lane == 0) mma_role<kBf16, G>(a, smem, b, tmem, items, count);
+    if (lane == 0) mma_role<kBf16, G>(a, smem, b, tmem, items, count, warp - kMmaWarp);
   }
   tc_fence_before();
   __syncthreads();
