@@ -188,14 +188,22 @@ def time_e2e(torch, dw, steps, stream):
 
 
 def gpu_launches_per_step(w, decode_max_rows=16):
+    """Kernels one step launches, following the library's host-side choices:
+    append; decode unless the lengths rule out a decode-class sequence;
+    prefill (head_dim 128: one kernel that plans its own work list when at
+    most 128 entries can exist, else a planning kernel first; head_dim 64:
+    planning kernel + prefill kernel)."""
     G = w.num_q_heads // w.num_kv_heads
-    rows = w.query_lens * G
-    n = 0
-    if (rows <= decode_max_rows).any():
+    S, T = w.num_seqs, int(w.query_lens.sum())
+    max_q = int(w.query_lens.max())
+    n = 1  # append
+    qd = decode_max_rows // G
+    if qd >= 1 and T <= (S - 1) * max_q + qd:
         n += 1  # decode (splits merged in the same kernel)
-    n += 1  # append
-    if (rows > decode_max_rows).any():
-        n += 2  # prefill planning + persistent prefill
+    if max_q * G > decode_max_rows:
+        pair_tokens = 2 * (128 // G)
+        max_entries = -(-T // pair_tokens) + S
+        n += 1 if (w.head_dim == 128 and max_entries <= 128) else 2
     return n
 
 

@@ -395,10 +395,18 @@ int kshipra_paged_attention(void* out, const void* q_rot, const void* k_arena, c
   if ((rc = arena_map(&kmap, k_arena, dtype, head_dim, rows, 16))) return rc;
   if ((rc = arena_map(&vmap, v_arena, dtype, head_dim, rows, 16))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (a.ws_counters &&
-      (e = cudaMemsetAsync(a.ws_counters, 0, plan.counter_bytes, s)) != cudaSuccess)
-    return cuda_fail(e, "clearing split counters");
-  if ((e = launch_decode(a, kmap, vmap, s)) != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  // decode class: query_len x group <= decode_max_rows, i.e. query_len <= qd.
+  // The query lengths sum to num_tokens and none exceeds max_query_len, so
+  // when num_tokens > (num_seqs - 1) x max_query_len + qd no sequence can be
+  // of the decode class and the decode launch is left out.
+  const long long qd = a.decode_max_rows / a.group;
+  const bool any_decode =
+      qd >= 1 && static_cast<long long>(num_tokens) <= static_cast<long long>(num_seqs - 1) * max_query_len + qd;
+  if (any_decode) {
+    if (a.ws_counters && (e = cudaMemsetAsync(a.ws_counters, 0, plan.counter_bytes, s)) != cudaSuccess)
+      return cuda_fail(e, "clearing split counters");
+    if ((e = launch_decode(a, kmap, vmap, s)) != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  }
   // prefill class: any sequence with more rows than the decode kernel takes
   if (static_cast<long long>(max_query_len) * a.group > a.decode_max_rows) {
     CUtensorMap kmap_p, vmap_p;
