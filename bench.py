@@ -187,6 +187,13 @@ def time_e2e(torch, dw, steps, stream):
     return t0.elapsed_time(t1), h2d, d2h
 
 
+# DRAM bytes (read + write) of one decode_kernel launch on the llama-decode
+# workload, from the ncu capture summarised in
+# profiles/decode_kernel_llama-decode.md; reported only for that workload
+# and valid while the kernel is unchanged since that capture.
+DECODE_TRAFFIC_LLAMA_DECODE = 592319232 + 1428224
+
+
 def gpu_launches_per_step(w, decode_max_rows=16):
     """Kernels one step launches, following the library's host-side choices:
     append; decode unless the lengths rule out a decode-class sequence;
@@ -359,7 +366,8 @@ def gpu_arm(args, w):
                 "block_size": w.block_size, "kv_bytes_per_step": kv, "parallelism": "replicas" if world > 1 else "single",
                 "l2": "inputs larger than L2 (%.0f MB of KV per step)" % (kv / 1e6)},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk.get("hbm_gbs"),
-                         "unit": "GB/s", "frac": round(achieved / pk.get("hbm_gbs"), 4), "traffic": None,
+                         "unit": "GB/s", "frac": round(achieved / pk.get("hbm_gbs"), 4),
+                         "traffic": DECODE_TRAFFIC_LLAMA_DECODE if w.name == "llama-decode" else None,
                          "kernel": "paged attention call (decode_kernel, split combine inside)",
                          "ms_per_launch": round(att_ms, 5), "peak_source": pk_src},
             "append_ms_per_step": round(statistics.mean(app), 5),
