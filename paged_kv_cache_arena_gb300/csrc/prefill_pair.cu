@@ -73,7 +73,7 @@ struct Layout {
   static constexpr int kK = kPB + kPTile;
   static constexpr int kV = kK + kStages * kKStage;
   static constexpr int kBar = kV + kStages * kVStage;
-  static constexpr int kNumBars = 2 + 4 * kStages + 12 + 2;
+  static constexpr int kNumBars = 2 + 4 * kStages + 14 + 2;
   static constexpr int kPlan = kBar + kNumBars * 8 + 16;  // work list planned in the kernel
   static constexpr int kPlanSorted = kPlan;                 // [kSortCapacity] sorted entries
   static constexpr int kPlanBuf = kPlanSorted + kSortCapacity * 8;  // [kSortCapacity] listed entries
@@ -97,7 +97,8 @@ struct Bars {
   uint64_t* s_full;    // [2] both: S_x ready in TMEM
   uint64_t* s_free;    // [2] leader, 8 warp arrivals (4 per CTA): S_x read, its columns free
   uint64_t* p_full;    // [2] leader, 8 warp arrivals: P_x written to shared memory
-  uint64_t* p_free;    // [2] both: the PV MMAs reading P_x (and accumulating O_x) completed
+  uint64_t* p_free;    // [2][2] both: the PV MMAs reading keys 0-63 / 64-127 of P_x completed
+                       // (the second also: O_x holds this tile's PV)
   uint64_t* o_full;    // [2] both: O_x complete for the item
   uint64_t* o_free;    // [2] leader, 8 warp arrivals: O_x read by the epilogue
   uint64_t* drain;     // [2] leader: per issuer
@@ -116,7 +117,7 @@ __device__ __forceinline__ Bars bars_at(uint8_t* smem) {
   b.s_free = b.s_full + 2;
   b.p_full = b.s_free + 2;
   b.p_free = b.p_full + 2;
-  b.o_full = b.p_free + 2;
+  b.o_full = b.p_free + 4;
   b.o_free = b.o_full + 2;
   b.drain = b.o_free + 2;
   return b;
@@ -413,7 +414,8 @@ __device__ __forceinline__ void issue_qk(const Descs& dd, const Bars& b, uint32_
 // O_x (+)= P_x V.  P_x is K-major in shared memory like Q (keys 64 g .. in
 // 64-key region g); V is MN-major, one 64-column swizzle atom per CTA (the
 // leader's columns of O, then the peer's), 8-key row groups 1024 B apart,
-// 16 keys = 2048 B per step.  Then signal p_free[x] in both CTAs.
+// 16 keys = 2048 B per step.  Each half of P (64 keys) is released to the
+// softmax as soon as its MMAs complete.
 template <bool kBf16>
 __device__ __forceinline__ void issue_pv(const Descs& dd, const Bars& b, uint32_t tmem, int x, int st,
                                          bool accumulate) {
@@ -427,8 +429,9 @@ __device__ __forceinline__ void issue_pv(const Descs& dd, const Bars& b, uint32_
     const uint32_t p_off = ((kk >> 2) * L::kQRegion + (kk & 3) * 32) >> 4;
     umma_pair_ss_w(tmem + 2 * kTile + kTile * x, p_lo + p_off, dd.qk_hi, v_lo + ((kk * 16 * 128) >> 4), dd.v_hi,
                    kIdescPV, kk > 0 ? 1u : acc);
+    if (kk == 3) umma_commit_pair(&b.p_free[2 * x]);
   }
-  umma_commit_pair(&b.p_free[x]);
+  umma_commit_pair(&b.p_free[2 * x + 1]);
 }
 
 // The MMAs of query tile x (one issuing thread per tile, so that neither
@@ -638,12 +641,13 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
         m_ref = m_tile;
       }
       const float ms = (m_ref == kNegInf ? 0.f : m_ref) * c2;
-      // the previous tile's PV MMAs must be done with P_x (and with O_x,
-      // which may be rescaled below) before either is written
-      if (gt > 0 && !warp_wait(&b.p_free[x], (gt - 1) & 1, a.status)) { ok = false; break; }
+      // the previous tile's PV MMAs must be done with each half of P_x (and
+      // with O_x, which may be rescaled below) before it is written
+      if (gt > 0 && !warp_wait(&b.p_free[2 * x], (gt - 1) & 1, a.status)) { ok = false; break; }
       float sums[4] = {0.f, 0.f, 0.f, 0.f};
       exp_store<kBf16>(t0, c2, ms, sums, p_row, 0, r);
       exp_store<kBf16>(t1, c2, ms, sums, p_row, 1, r);
+      if (gt > 0 && !warp_wait(&b.p_free[2 * x + 1], (gt - 1) & 1, a.status)) { ok = false; break; }
       exp_store<kBf16>(t2, c2, ms, sums, p_row, 2, r);
       exp_store<kBf16>(t3, c2, ms, sums, p_row, 3, r);
       l = fmaf(l, alpha, (sums[0] + sums[1]) + (sums[2] + sums[3]));
@@ -748,7 +752,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&b.s_full[i], 1);
       mbar_init(&b.s_free[i], 2 * 4);  // four softmax warps per tile in each CTA
       mbar_init(&b.p_full[i], 2 * 4);
-      mbar_init(&b.p_free[i], 1);
+      mbar_init(&b.p_free[2 * i], 1);
+      mbar_init(&b.p_free[2 * i + 1], 1);
       mbar_init(&b.o_full[i], 1);
       mbar_init(&b.o_free[i], 2 * 4);
     }
