@@ -126,18 +126,33 @@ def _events(torch, n):
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
 
-def time_steps(torch, dw, steps, warmup, stream, flush=None):
-    """Times `steps` whole steps (append + attention) on `stream`.
+def time_steps(torch, dw, steps, warmup, stream, flush=None, fused=False):
+    """Times `steps` whole steps on `stream`: append + attention as two calls,
+    or (fused) one kshipra_decode_step call.
 
-    Returns (total_ms, per-step append ms list, per-step attention ms list).
-    Events bracket each call on the launching stream.  When `flush` is given
-    (a byte buffer larger than L2), it is overwritten between steps, outside
-    the timed windows.
+    Returns (total_ms, per-step append ms list, per-step attention ms list);
+    for a fused step the append list is empty and the attention list holds
+    the whole call.  Events bracket each call on the launching stream.  When
+    `flush` is given (a byte buffer larger than L2), it is overwritten between
+    steps, outside the timed windows.
     """
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            dw.step(stream=stream)
+            dw.decode_step(stream=stream) if fused else dw.step(stream=stream)
     torch.cuda.synchronize()
+    if fused:
+        ev = _events(torch, 2 * steps)
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                if flush is not None:
+                    flush.fill_(i & 0xFF)
+                ev[2 * i].record(stream)
+                dw.decode_step(stream=stream)
+                ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        att = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)]
+        total = ev[0].elapsed_time(ev[-1]) if flush is None else sum(att)
+        return total, [], att
     ev = _events(torch, 3 * steps)
     t0, t1 = _events(torch, 2)
     with torch.cuda.stream(stream):
@@ -161,9 +176,10 @@ def time_steps(torch, dw, steps, warmup, stream, flush=None):
     return total, app, att
 
 
-def time_e2e(torch, dw, steps, stream):
+def time_e2e(torch, dw, steps, stream, fused=False):
     """Same step through the public API from pinned host buffers: H2D of the
-    step's inputs, append + attention, D2H of the output, every step."""
+    step's inputs, the step (fused or two calls), D2H of the output, every
+    step."""
     w = dw.w
     host = {}
     for name in ("q", "k_new", "v_new", "block_tables", "context_lens", "query_start_loc", "positions"):
@@ -179,7 +195,7 @@ def time_e2e(torch, dw, steps, stream):
         for _ in range(steps):
             for name, h in host.items():
                 getattr(dw, name).copy_(h, non_blocking=True)
-            dw.step(stream=stream)
+            dw.decode_step(stream=stream) if fused else dw.step(stream=stream)
             out_host.copy_(dw.out, non_blocking=True)
             stream.synchronize()  # the caller reads the result every step
         t1.record(stream)
@@ -188,21 +204,26 @@ def time_e2e(torch, dw, steps, stream):
 
 
 # DRAM bytes (read + write) of one decode_kernel launch on the llama-decode
-# workload, from the ncu capture summarised in
-# profiles/decode_kernel_llama-decode.md; reported only for that workload
-# and valid while the kernel is unchanged since that capture.
-DECODE_TRAFFIC_LLAMA_DECODE = 592319232 + 1428224
+# workload, from the ncu captures summarised in
+# profiles/decode_kernel_llama-decode.md (the fused step's kernel, and the
+# attention-only kernel of the two-call step); reported only for that
+# workload and valid while the kernel is unchanged since its capture.
+DECODE_TRAFFIC_LLAMA_DECODE = 592425472 + 2235648
+DECODE_TRAFFIC_LLAMA_DECODE_TWO_CALL = 592319232 + 1428224
 
 
-def gpu_launches_per_step(w, decode_max_rows=16):
+def gpu_launches_per_step(w, decode_max_rows=16, fused=False):
     """Kernels one step launches, following the library's host-side choices:
     append; decode unless the lengths rule out a decode-class sequence;
     prefill (head_dim 128: one kernel that plans its own work list when at
     most 128 entries can exist, else a planning kernel first; head_dim 64:
-    planning kernel + prefill kernel)."""
+    planning kernel + prefill kernel); a fused decode step of a decode-class
+    batch is one launch."""
     G = w.num_q_heads // w.num_kv_heads
     S, T = w.num_seqs, int(w.query_lens.sum())
     max_q = int(w.query_lens.max())
+    if fused and max_q * G <= decode_max_rows:
+        return 1  # kshipra_decode_step: RoPE-and-append inside the decode kernel
     n = 1  # append
     qd = decode_max_rows // G
     if qd >= 1 and T <= (S - 1) * max_q + qd:
@@ -319,6 +340,7 @@ def gpu_arm(args, w):
     dw = DeviceWorkload(w)
     stream = torch.cuda.Stream()
     kv = decode_kv_bytes(w)
+    fused = args.step == "fused"
     try:
         smi_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:
@@ -327,7 +349,7 @@ def gpu_arm(args, w):
     torch.cuda.synchronize()
     with ClockSampler(smi_id) as clk:
         barrier()
-        total_ms, app, att = time_steps(torch, dw, args.steps, args.warmup, stream)
+        total_ms, app, att = time_steps(torch, dw, args.steps, args.warmup, stream, fused=fused)
         barrier()
     clocks = clk.summary()
     if world > 1:
@@ -340,7 +362,7 @@ def gpu_arm(args, w):
     att_ms = statistics.mean(att)
     achieved = kv / (att_ms * 1e-3) / 1e9
     e2e_steps = min(args.steps, 300)
-    e2e_ms, h2d, d2h = time_e2e(torch, dw, e2e_steps, stream)
+    e2e_ms, h2d, d2h = time_e2e(torch, dw, e2e_steps, stream, fused=fused)
     e2e_value = world * kv * e2e_steps / (e2e_ms * 1e-3) / 1e9
     secondary = None
     if not args.no_prefill:
@@ -353,7 +375,7 @@ def gpu_arm(args, w):
         secs, kv_s, _, n_s, threads = oracle_sample(w)
         cpu = {"value": round(kv_s / secs / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": "%d of %d sequences, all q heads, float64 C oracle, %.1f s" % (n_s, w.num_seqs, secs)}
-    launches = gpu_launches_per_step(w) * args.steps
+    launches = gpu_launches_per_step(w, fused=fused) * args.steps
     if rank == 0:
         line = {
             "metric": "decode KV-read GB/s", "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -367,10 +389,13 @@ def gpu_arm(args, w):
                 "l2": "inputs larger than L2 (%.0f MB of KV per step)" % (kv / 1e6)},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk.get("hbm_gbs"),
                          "unit": "GB/s", "frac": round(achieved / pk.get("hbm_gbs"), 4),
-                         "traffic": DECODE_TRAFFIC_LLAMA_DECODE if w.name == "llama-decode" else None,
-                         "kernel": "paged attention call (decode_kernel, split combine inside)",
+                         "traffic": (DECODE_TRAFFIC_LLAMA_DECODE if fused else DECODE_TRAFFIC_LLAMA_DECODE_TWO_CALL)
+                         if w.name == "llama-decode" else None,
+                         "kernel": ("decode step (decode_kernel with RoPE-and-append and split combine inside)"
+                                    if fused else "paged attention call (decode_kernel, split combine inside)"),
                          "ms_per_launch": round(att_ms, 5), "peak_source": pk_src},
-            "append_ms_per_step": round(statistics.mean(app), 5),
+            "append_ms_per_step": round(statistics.mean(app), 5) if app else 0.0,
+            "step": "one kshipra_decode_step launch" if fused else "kshipra_kv_append_rope + kshipra_paged_attention",
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": launches, "clocks": clocks, "device_status": status,
@@ -389,6 +414,8 @@ def main():
     ap.add_argument("--impl", choices=["kshipra", "reference"], default="kshipra")
     ap.add_argument("--workload", default="llama-decode", choices=["llama-decode", "long-decode", "mixed"])
     ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill secondary object")
+    ap.add_argument("--step", choices=["fused", "two-call"], default="fused",
+                    help="a decode step as one kshipra_decode_step launch or as append + attention calls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

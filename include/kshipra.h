@@ -178,6 +178,33 @@ int kshipra_paged_attention(void* out, const void* q_rot, const void* k_arena, c
                             void* stream);
 
 /*
+ * One decode step: kshipra_kv_append_rope followed by
+ * kshipra_paged_attention (kshipra-3, sections 1 and 4), with the same
+ * arguments and results -- the arena gets the new tokens' rotated K and raw V
+ * bit for bit as the append writes them, out is the attention of the
+ * rotated q -- in ONE launch when every sequence is of the decode class
+ * (max_query_len x group <= KSHIPRA_OPT_DECODE_MAX_ROWS): each decode CTA
+ * rotates its query rows from q in registers, and the CTA whose key split
+ * holds a new token's position writes that token's K and V before it reads
+ * the arena.  Otherwise the two calls run one after the other.
+ *
+ * q [num_tokens][num_q_heads][head_dim], k, v [num_tokens][num_kv_heads]
+ * [head_dim], rope_table as for kshipra_kv_append_rope; the other arguments
+ * as for kshipra_paged_attention, with the same workspace size.  q_rot
+ * (device, [num_tokens][num_q_heads][head_dim]) receives the rotated q; it
+ * may be NULL on the one-launch path and is required otherwise.  q_rot must
+ * not alias out or q.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA.
+ */
+int kshipra_decode_step(void* out, const void* q, const void* k, const void* v, void* q_rot, void* k_arena,
+                       void* v_arena, const int32_t* block_tables, const int32_t* context_lens,
+                       const int32_t* query_start_loc, const int32_t* positions, const float* rope_table,
+                       int rope_max_pos, int num_seqs, int num_tokens, int max_query_len, int max_context_len,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                       int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/*
  * Paged attention without any allocation and without a caller workspace.
  * The paper has no counterpart; this is a convenience of this library.
  *

@@ -122,6 +122,22 @@ def kshipra_paged_attention(out, q_rot, k_arena, v_arena, block_tables, context_
         float(scale), _dtype_code(q_rot), _ptr(workspace), ws_bytes, _stream(stream)), "kshipra_paged_attention")
 
 
+def kshipra_decode_step(out, q, k, v, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc,
+                        positions, rope_table, max_query_len: int, max_context_len: int, scale: float,
+                        workspace=None, stream=None) -> None:
+    """RoPE-and-append then attention in one launch for decode-class batches
+    (q_rot may then be None); shapes as in include/kshipra.h."""
+    num_tokens, num_q_heads, head_dim = q.shape
+    num_blocks, num_kv_heads, block_size, _ = k_arena.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.load().kshipra_decode_step(
+        _ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(q_rot), _ptr(k_arena), _ptr(v_arena), _ptr(block_tables),
+        _ptr(context_lens), _ptr(query_start_loc), _ptr(positions), _ptr(rope_table), rope_table.shape[0],
+        query_start_loc.shape[0] - 1, num_tokens, max_query_len, max_context_len, num_q_heads, num_kv_heads,
+        head_dim, block_size, block_tables.shape[1], num_blocks, float(scale), _dtype_code(q), _ptr(workspace),
+        ws_bytes, _stream(stream)), "kshipra_decode_step")
+
+
 def kshipra_paged_attention_noalloc(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc,
                                     positions, max_query_len: int, max_context_len: int, scale: float,
                                     stream=None) -> None:

@@ -20,6 +20,7 @@ EXPORTS = (
     "kshipra_kv_append_rope",
     "kshipra_paged_attention_workspace_size",
     "kshipra_paged_attention",
+    "kshipra_decode_step",
     "kshipra_paged_attention_noalloc",
     "kshipra_device_status",
     "kshipra_set_option",
@@ -47,6 +48,8 @@ def load() -> ctypes.CDLL:
         lib.kshipra_kv_append_rope.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P]
         lib.kshipra_paged_attention_workspace_size.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(SZ)]
         lib.kshipra_paged_attention.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, P, SZ, P]
+        lib.kshipra_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, F, I,
+                                            P, SZ, P]
         lib.kshipra_paged_attention_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I,
                                                         P]
         lib.kshipra_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), P]

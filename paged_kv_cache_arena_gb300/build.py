@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkshipra.so")
 SOURCES = ("api.cu", "append_rope.cu", "decode.cu", "prefill.cu", "prefill_pair.cu", "noalloc.cu")
-HEADERS = ("common.cuh", "internal.h")
+HEADERS = ("common.cuh", "internal.h", "rope.cuh")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]

@@ -205,6 +205,115 @@ WorkspacePlan plan_workspace(int num_seqs, int num_tokens, int max_context_len, 
   return p;
 }
 
+// The new tokens' raw rows for the fused decode step (see AttnArgs).
+struct FusedInputs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* rope_table;
+  int rope_max_pos;
+  void* q_rot_out;
+  void* k_arena;
+  void* v_arena;
+};
+
+// kshipra_paged_attention, or with fz the fused decode step (every sequence
+// of the decode class; q_rot then is an optional output).
+int attention_impl(void* out, const void* q_rot, const void* k_arena, const void* v_arena,
+                   const int32_t* block_tables, const int32_t* context_lens, const int32_t* query_start_loc,
+                   const int32_t* positions, int num_seqs, int num_tokens, int max_query_len, int max_context_len,
+                   int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                   int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream,
+                   const FusedInputs* fz) {
+  if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || max_context_len < 0)
+    return fail(KSHIPRA_ERR_INVALID_ARG, "negative size argument");
+  if (num_seqs == 0 && num_tokens > 0) return fail(KSHIPRA_ERR_INVALID_ARG, "tokens without sequences");
+  int rc = check_heads(num_q_heads, num_kv_heads, head_dim, block_size, dtype);
+  if (rc) return rc;
+  if ((rc = check_arena(num_blocks, num_kv_heads, block_size, max_blocks_per_seq))) return rc;
+  if (num_seqs >= (1 << 24) || max_query_len / (2 * (128 / (num_q_heads / num_kv_heads))) >= (1 << 16))
+    return fail(KSHIPRA_ERR_UNSUPPORTED, "num_seqs must stay below 2^24 and max_query_len below 2^16 tile pairs");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(KSHIPRA_ERR_INVALID_ARG, "scale must be positive");
+  if (num_tokens == 0) return KSHIPRA_OK;
+  if (max_context_len <= 0 || max_query_len <= 0)
+    return fail(KSHIPRA_ERR_INVALID_ARG, "max_context_len and max_query_len must be positive");
+  if (static_cast<long long>(max_context_len) > static_cast<long long>(max_blocks_per_seq) * block_size)
+    return fail(KSHIPRA_ERR_INVALID_ARG, "max_context_len %d exceeds max_blocks_per_seq x block_size",
+                max_context_len);
+  if (!out || (!q_rot && !fz) || !k_arena || !v_arena || !block_tables || !context_lens || !query_start_loc ||
+      !positions)
+    return fail(KSHIPRA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (out == q_rot) return fail(KSHIPRA_ERR_INVALID_ARG, "out must not alias q_rot");
+  const void* vec[] = {out, q_rot, k_arena, v_arena};
+  for (const void* p : vec)
+    if (p && !aligned(p, 16)) return fail(KSHIPRA_ERR_INVALID_ARG, "data pointers must be 16-byte aligned");
+  int sms = 0;
+  cudaError_t e = sm_count_current(&sms);
+  if (e != cudaSuccess) return cuda_fail(e, "SM count");
+  const WorkspacePlan plan =
+      plan_workspace(num_seqs, num_tokens, max_context_len, num_q_heads, num_kv_heads, head_dim, sms);
+  if (workspace_bytes < plan.total)
+    return fail(KSHIPRA_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, %zu needed", workspace_bytes, plan.total);
+  if (plan.total && (!workspace || !aligned(workspace, 256)))
+    return fail(KSHIPRA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
+
+  AttnArgs a{};
+  a.out = out; a.q_rot = q_rot; a.block_tables = block_tables; a.context_lens = context_lens;
+  a.query_start_loc = query_start_loc; a.positions = positions;
+  char* ws = static_cast<char*>(workspace);
+  a.ws_o = plan.o_bytes ? reinterpret_cast<float*>(ws) : nullptr;
+  a.ws_ml = plan.ml_bytes ? reinterpret_cast<float*>(ws + plan.o_bytes) : nullptr;
+  a.ws_counters = plan.counter_bytes ? reinterpret_cast<unsigned*>(ws + plan.o_bytes + plan.ml_bytes) : nullptr;
+  const size_t items_off = plan.o_bytes + plan.ml_bytes + plan.counter_bytes;
+  a.ws_items = plan.items_bytes ? reinterpret_cast<uint64_t*>(ws + items_off) : nullptr;
+  a.ws_item_count =
+      plan.items_bytes ? reinterpret_cast<int*>(ws + items_off + static_cast<size_t>(plan.max_items) * 8) : nullptr;
+  a.max_items = plan.max_items;
+  a.sm_count = sms;
+  a.num_seqs = num_seqs; a.num_tokens = num_tokens; a.max_query_len = max_query_len;
+  a.max_context_len = max_context_len; a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
+  a.group = num_q_heads / num_kv_heads; a.head_dim = head_dim; a.block_size = block_size;
+  a.max_blocks_per_seq = max_blocks_per_seq; a.num_blocks = num_blocks;
+  a.split_tokens = plan.split_tokens; a.max_splits = plan.max_splits;
+  a.decode_max_rows = g_opt_decode_max_rows.load();
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.dtype = dtype;
+  if (fz) {
+    a.q_raw = fz->q; a.k_new = fz->k; a.v_new = fz->v; a.rope_table = fz->rope_table;
+    a.rope_max_pos = fz->rope_max_pos; a.q_rot_out = fz->q_rot_out;
+    a.k_arena_w = fz->k_arena; a.v_arena_w = fz->v_arena;
+  }
+  if ((e = status_ptr(&a.status)) != cudaSuccess) return cuda_fail(e, "status word");
+
+  const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
+  CUtensorMap kmap, vmap, qmap;
+  if ((rc = arena_map(&kmap, k_arena, dtype, head_dim, rows, 16))) return rc;
+  if ((rc = arena_map(&vmap, v_arena, dtype, head_dim, rows, 16))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // decode class: query_len x group <= decode_max_rows, i.e. query_len <= qd.
+  // The query lengths sum to num_tokens and none exceeds max_query_len, so
+  // when num_tokens > (num_seqs - 1) x max_query_len + qd no sequence can be
+  // of the decode class and the decode launch is left out.
+  const long long qd = a.decode_max_rows / a.group;
+  const bool any_decode =
+      qd >= 1 && static_cast<long long>(num_tokens) <= static_cast<long long>(num_seqs - 1) * max_query_len + qd;
+  if (any_decode) {
+    if (a.ws_counters && (e = cudaMemsetAsync(a.ws_counters, 0, plan.counter_bytes, s)) != cudaSuccess)
+      return cuda_fail(e, "clearing split counters");
+    if ((e = launch_decode(a, kmap, vmap, s)) != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  }
+  // prefill class: any sequence with more rows than the decode kernel takes
+  if (static_cast<long long>(max_query_len) * a.group > a.decode_max_rows) {
+    CUtensorMap kmap_p, vmap_p;
+    if ((rc = arena_map(&kmap_p, k_arena, dtype, head_dim, rows, block_size))) return rc;
+    if ((rc = arena_map(&vmap_p, v_arena, dtype, head_dim, rows, block_size))) return rc;
+    if ((rc = query_map(&qmap, q_rot, dtype, head_dim, num_q_heads, num_tokens, a.group))) return rc;
+    if ((e = launch_prefill(a, kmap_p, vmap_p, qmap, s)) != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
+  }
+  return KSHIPRA_OK;
+}
+
+
 }  // namespace
 
 // ===========================================================================
@@ -336,86 +445,49 @@ int kshipra_paged_attention(void* out, const void* q_rot, const void* k_arena, c
                             int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes,
                             void* stream) {
   g_last_error[0] = 0;
-  if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || max_context_len < 0)
-    return fail(KSHIPRA_ERR_INVALID_ARG, "negative size argument");
-  if (num_seqs == 0 && num_tokens > 0) return fail(KSHIPRA_ERR_INVALID_ARG, "tokens without sequences");
+  return attention_impl(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc, positions,
+                        num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads, num_kv_heads, head_dim,
+                        block_size, max_blocks_per_seq, num_blocks, scale, dtype, workspace, workspace_bytes, stream,
+                        nullptr);
+}
+
+int kshipra_decode_step(void* out, const void* q, const void* k, const void* v, void* q_rot, void* k_arena,
+                       void* v_arena, const int32_t* block_tables, const int32_t* context_lens,
+                       const int32_t* query_start_loc, const int32_t* positions, const float* rope_table,
+                       int rope_max_pos, int num_seqs, int num_tokens, int max_query_len, int max_context_len,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                       int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  g_last_error[0] = 0;
   int rc = check_heads(num_q_heads, num_kv_heads, head_dim, block_size, dtype);
   if (rc) return rc;
-  if ((rc = check_arena(num_blocks, num_kv_heads, block_size, max_blocks_per_seq))) return rc;
-  if (num_seqs >= (1 << 24) || max_query_len / (2 * (128 / (num_q_heads / num_kv_heads))) >= (1 << 16))
-    return fail(KSHIPRA_ERR_UNSUPPORTED, "num_seqs must stay below 2^24 and max_query_len below 2^16 tile pairs");
-  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(KSHIPRA_ERR_INVALID_ARG, "scale must be positive");
-  if (num_tokens == 0) return KSHIPRA_OK;
-  if (max_context_len <= 0 || max_query_len <= 0)
-    return fail(KSHIPRA_ERR_INVALID_ARG, "max_context_len and max_query_len must be positive");
-  if (static_cast<long long>(max_context_len) > static_cast<long long>(max_blocks_per_seq) * block_size)
-    return fail(KSHIPRA_ERR_INVALID_ARG, "max_context_len %d exceeds max_blocks_per_seq x block_size",
-                max_context_len);
-  if (!out || !q_rot || !k_arena || !v_arena || !block_tables || !context_lens || !query_start_loc || !positions)
+  if (rope_max_pos <= 0) return fail(KSHIPRA_ERR_INVALID_ARG, "rope_max_pos must be positive");
+  if (num_tokens > 0 && (!q || !k || !v || !rope_table))
     return fail(KSHIPRA_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (out == q_rot) return fail(KSHIPRA_ERR_INVALID_ARG, "out must not alias q_rot");
-  const void* vec[] = {out, q_rot, k_arena, v_arena};
+  const void* vec[] = {q, k, v, q_rot, rope_table};
   for (const void* p : vec)
-    if (!aligned(p, 16)) return fail(KSHIPRA_ERR_INVALID_ARG, "data pointers must be 16-byte aligned");
-  int sms = 0;
-  cudaError_t e = sm_count_current(&sms);
-  if (e != cudaSuccess) return cuda_fail(e, "SM count");
-  const WorkspacePlan plan =
-      plan_workspace(num_seqs, num_tokens, max_context_len, num_q_heads, num_kv_heads, head_dim, sms);
-  if (workspace_bytes < plan.total)
-    return fail(KSHIPRA_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, %zu needed", workspace_bytes, plan.total);
-  if (plan.total && (!workspace || !aligned(workspace, 256)))
-    return fail(KSHIPRA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
-
-  AttnArgs a{};
-  a.out = out; a.q_rot = q_rot; a.block_tables = block_tables; a.context_lens = context_lens;
-  a.query_start_loc = query_start_loc; a.positions = positions;
-  char* ws = static_cast<char*>(workspace);
-  a.ws_o = plan.o_bytes ? reinterpret_cast<float*>(ws) : nullptr;
-  a.ws_ml = plan.ml_bytes ? reinterpret_cast<float*>(ws + plan.o_bytes) : nullptr;
-  a.ws_counters = plan.counter_bytes ? reinterpret_cast<unsigned*>(ws + plan.o_bytes + plan.ml_bytes) : nullptr;
-  const size_t items_off = plan.o_bytes + plan.ml_bytes + plan.counter_bytes;
-  a.ws_items = plan.items_bytes ? reinterpret_cast<uint64_t*>(ws + items_off) : nullptr;
-  a.ws_item_count =
-      plan.items_bytes ? reinterpret_cast<int*>(ws + items_off + static_cast<size_t>(plan.max_items) * 8) : nullptr;
-  a.max_items = plan.max_items;
-  a.sm_count = sms;
-  a.num_seqs = num_seqs; a.num_tokens = num_tokens; a.max_query_len = max_query_len;
-  a.max_context_len = max_context_len; a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
-  a.group = num_q_heads / num_kv_heads; a.head_dim = head_dim; a.block_size = block_size;
-  a.max_blocks_per_seq = max_blocks_per_seq; a.num_blocks = num_blocks;
-  a.split_tokens = plan.split_tokens; a.max_splits = plan.max_splits;
-  a.decode_max_rows = g_opt_decode_max_rows.load();
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.dtype = dtype;
-  if ((e = status_ptr(&a.status)) != cudaSuccess) return cuda_fail(e, "status word");
-
-  const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
-  CUtensorMap kmap, vmap, qmap;
-  if ((rc = arena_map(&kmap, k_arena, dtype, head_dim, rows, 16))) return rc;
-  if ((rc = arena_map(&vmap, v_arena, dtype, head_dim, rows, 16))) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // decode class: query_len x group <= decode_max_rows, i.e. query_len <= qd.
-  // The query lengths sum to num_tokens and none exceeds max_query_len, so
-  // when num_tokens > (num_seqs - 1) x max_query_len + qd no sequence can be
-  // of the decode class and the decode launch is left out.
-  const long long qd = a.decode_max_rows / a.group;
-  const bool any_decode =
-      qd >= 1 && static_cast<long long>(num_tokens) <= static_cast<long long>(num_seqs - 1) * max_query_len + qd;
-  if (any_decode) {
-    if (a.ws_counters && (e = cudaMemsetAsync(a.ws_counters, 0, plan.counter_bytes, s)) != cudaSuccess)
-      return cuda_fail(e, "clearing split counters");
-    if ((e = launch_decode(a, kmap, vmap, s)) != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    if (p && !aligned(p, 16)) return fail(KSHIPRA_ERR_INVALID_ARG, "data pointers must be 16-byte aligned");
+  if (q_rot && (q_rot == out || q_rot == q)) return fail(KSHIPRA_ERR_INVALID_ARG, "q_rot must not alias out or q");
+  const int group = num_q_heads / num_kv_heads;
+  if (static_cast<long long>(max_query_len) * group > g_opt_decode_max_rows.load()) {
+    // rows for the tensor-core prefill kernel: the two steps, through q_rot
+    if (!q_rot)
+      return fail(KSHIPRA_ERR_INVALID_ARG, "q_rot is required when a sequence has more than %d query rows",
+                  g_opt_decode_max_rows.load());
+    if ((rc = kshipra_kv_append_rope(q, k, v, q_rot, k_arena, v_arena, block_tables, query_start_loc, positions,
+                                     rope_table, rope_max_pos, num_seqs, num_tokens, num_q_heads, num_kv_heads,
+                                     head_dim, block_size, max_blocks_per_seq, num_blocks, dtype, stream)))
+      return rc;
+    return kshipra_paged_attention(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc,
+                                   positions, num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads,
+                                   num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype,
+                                   workspace, workspace_bytes, stream);
   }
-  // prefill class: any sequence with more rows than the decode kernel takes
-  if (static_cast<long long>(max_query_len) * a.group > a.decode_max_rows) {
-    CUtensorMap kmap_p, vmap_p;
-    if ((rc = arena_map(&kmap_p, k_arena, dtype, head_dim, rows, block_size))) return rc;
-    if ((rc = arena_map(&vmap_p, v_arena, dtype, head_dim, rows, block_size))) return rc;
-    if ((rc = query_map(&qmap, q_rot, dtype, head_dim, num_q_heads, num_tokens, a.group))) return rc;
-    if ((e = launch_prefill(a, kmap_p, vmap_p, qmap, s)) != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
-  }
-  return KSHIPRA_OK;
+  const FusedInputs fz{q, k, v, rope_table, rope_max_pos, q_rot, k_arena, v_arena};
+  return attention_impl(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc, positions,
+                        num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads, num_kv_heads, head_dim,
+                        block_size, max_blocks_per_seq, num_blocks, scale, dtype, workspace, workspace_bytes, stream,
+                        &fz);
 }
 
 }  // extern "C"

@@ -7,51 +7,21 @@
 // and section 4 (RoPE at absolute positions: a chunk after P cached tokens
 // starts at position P).
 //
-// One warp per (token, head).  The rotation is done in float32 from the
-// caller's (cos, sin) table with separately rounded products and one add,
+// One warp per (token, head).  The rotation (rope.cuh) is done in float32 from
+// the caller's (cos, sin) table with separately rounded products and one add,
 // then rounded once to the storage type, so the arena image is reproducible
 // bit for bit.  (float32 keeps the step off GB300's slow FP64 units.)  The
 // volume is small (num_tokens x (Hq + Hkv) x head_dim elements per call); the
 // kernel is memory-latency bound and far from the hot path's cost.
 #include "common.cuh"
 #include "internal.h"
+#include "rope.cuh"
 
 namespace kshipra {
 namespace {
 
 constexpr int kAppendWarps = 4;
 constexpr int kAppendThreads = 32 * kAppendWarps;
-
-// Storage bits -> float32 (exact).
-template <bool kBf16>
-__device__ __forceinline__ float bits_to_float(uint32_t h) {
-  if constexpr (kBf16)
-    return __uint_as_float(h << 16);
-  else
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
-}
-
-// Rotates pairs (i, i + d/2) and (i + 1, i + 1 + d/2) of one head row:
-//   y_i = x_i c - x_{i+d/2} s,  y_{i+d/2} = x_{i+d/2} c + x_i s
-// with separately rounded float32 products and one rounded add or subtract,
-// then one rounding to the storage type.
-template <bool kBf16>
-__device__ __forceinline__ void rotate_two_pairs(const uint16_t* src, uint16_t* dst, int i, int half,
-                                                 const float* cs) {
-  const uint32_t lo = *reinterpret_cast<const uint32_t*>(src + i);
-  const uint32_t hi = *reinterpret_cast<const uint32_t*>(src + i + half);
-  const float4 t = *reinterpret_cast<const float4*>(cs + 2 * i);  // c_i, s_i, c_i+1, s_i+1
-  const float x0 = bits_to_float<kBf16>(lo & 0xFFFF), x1 = bits_to_float<kBf16>(lo >> 16);
-  const float y0 = bits_to_float<kBf16>(hi & 0xFFFF), y1 = bits_to_float<kBf16>(hi >> 16);
-  const float a0 = __fsub_rn(__fmul_rn(x0, t.x), __fmul_rn(y0, t.y));
-  const float b0 = __fadd_rn(__fmul_rn(y0, t.x), __fmul_rn(x0, t.y));
-  const float a1 = __fsub_rn(__fmul_rn(x1, t.z), __fmul_rn(y1, t.w));
-  const float b1 = __fadd_rn(__fmul_rn(y1, t.z), __fmul_rn(x1, t.w));
-  *reinterpret_cast<uint32_t*>(dst + i) =
-      static_cast<uint32_t>(round_f32<kBf16>(a0)) | (static_cast<uint32_t>(round_f32<kBf16>(a1)) << 16);
-  *reinterpret_cast<uint32_t*>(dst + i + half) =
-      static_cast<uint32_t>(round_f32<kBf16>(b0)) | (static_cast<uint32_t>(round_f32<kBf16>(b1)) << 16);
-}
 
 // One warp per (token, head): warps of blockIdx.y cover q heads first, then
 // kv heads (k rotated into the arena, v copied).  Lane i rotates pairs 2i and

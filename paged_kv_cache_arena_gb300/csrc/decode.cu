@@ -27,10 +27,17 @@
 //    rounded output directly, otherwise the partial (m, l, o) goes to the
 //    workspace, and the CTA that finishes last for its (sequence, kv head)
 //    (atomic ticket) merges all splits.
+//  - Fused decode step (kshipra_decode_step): the kernel also does the
+//    RoPE-and-append of the step's new tokens.  Each CTA rotates its own query
+//    rows from the raw q in registers; the CTA whose split holds a new token's
+//    position writes that token's rotated K and raw V (its kv head) into the
+//    arena before it loads anything -- no other CTA reads that position -- so
+//    the step is one launch.  The rotation is the append kernel's, bit for bit.
 #include <float.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "rope.cuh"
 
 namespace kshipra {
 namespace {
@@ -40,6 +47,12 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 3;
 constexpr int kChunk = 16;  // keys per stage
 constexpr float kNegInf = -INFINITY;
+
+// Generic-proxy global writes of this thread ordered before later async-proxy
+// (TMA) reads that a barrier orders after them.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 template <int D>
 struct DecodeLayout {
@@ -57,10 +70,11 @@ struct DecodeLayout {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-template <int D, bool kBf16, int NT>
+template <int D, bool kBf16, bool kFused, int NT>
 __device__ __forceinline__ void decode_body(const CUtensorMap* kmap, const CUtensorMap* vmap, const AttnArgs& a,
-                                            uint8_t* smem, int s, int h, int split, int q0, int nrows, int ctx,
+                                            uint8_t* smem, int s, int h, int split, int q0, int qlen, int ctx,
                                             int nsplit) {
+  const int nrows = qlen * a.group;
   using L = DecodeLayout<D>;
   constexpr int KS = D / 16;  // 16-wide steps over the head dimension
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -74,6 +88,51 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* kmap, const CUten
   const int nchunks = ceil_div(tok_end - tok_begin, kChunk);
   const int my_chunks = nchunks > warp ? ceil_div(nchunks - warp, kWarps) : 0;
   const int oob_row = a.num_blocks * a.num_kv_heads * a.block_size;  // past the tensor: zero fill
+
+  if constexpr (kFused) {
+    // the step's new tokens whose positions fall in this split: rotated K and
+    // raw V of kv head h into their arena slots, one warp per token, before
+    // this CTA loads any tile
+    constexpr int half = D / 2;
+    bool wrote = false;
+    for (int i = warp; i < qlen; i += kWarps) {
+      const int t = q0 + i;
+      const int pos = __ldg(a.positions + t);
+      if (pos < tok_begin || pos >= tok_end) continue;
+      if (pos >= a.rope_max_pos) {
+        if (lane == 0) report(a.status, KSHIPRA_DEV_BAD_POSITION);
+        continue;
+      }
+      const int blk = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + pos / a.block_size);
+      if (blk < 0 || blk >= a.num_blocks) {
+        if (lane == 0) report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
+        continue;
+      }
+      const size_t src = (static_cast<size_t>(t) * a.num_kv_heads + h) * D;
+      const size_t dst = ((static_cast<size_t>(blk) * a.num_kv_heads + h) * a.block_size + pos % a.block_size) * D;
+      if (2 * lane < half)
+        rotate_two_pairs<kBf16>(static_cast<const uint16_t*>(a.k_new) + src, static_cast<uint16_t*>(a.k_arena_w) + dst,
+                                2 * lane, half, a.rope_table + static_cast<size_t>(pos) * D);
+      if (lane < D / 8)  // value row: bit copy in 16-byte pieces
+        reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.v_arena_w) + dst)[lane] =
+            reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v_new) + src)[lane];
+      wrote = true;
+    }
+    if (wrote) fence_proxy_async_global();  // the rows above, before the tile loads below
+    __syncthreads();
+    // split 0 also stores the rotated query rows when asked to
+    if (split == 0 && a.q_rot_out != nullptr)
+      for (int n = warp; n < nrows; n += kWarps) {
+        const int t = q0 + n / a.group;
+        const int pos = __ldg(a.positions + t);
+        if (pos < 0 || pos >= a.rope_max_pos) continue;
+        const size_t row = (static_cast<size_t>(t) * a.num_q_heads + h * a.group + n % a.group) * D;
+        if (2 * lane < half)
+          rotate_two_pairs<kBf16>(static_cast<const uint16_t*>(a.q_raw) + row,
+                                  static_cast<uint16_t*>(a.q_rot_out) + row, 2 * lane, half,
+                                  a.rope_table + static_cast<size_t>(pos) * D);
+      }
+  }
 
   if (lane == 0) {
     for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
@@ -110,17 +169,38 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* kmap, const CUten
   // query row 8 nt + g = (token q0 + n / G, q head h G + n % G).
   uint32_t qb[NT][KS][2];
   int rpos[NT][2];
-  const uint16_t* qrot = static_cast<const uint16_t*>(a.q_rot);
+  const uint16_t* qrot = static_cast<const uint16_t*>(kFused ? a.q_raw : a.q_rot);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int n = 8 * nt + g;
     const uint16_t* qp = nullptr;
     if (n < nrows)
       qp = qrot + (static_cast<size_t>(q0 + n / G) * a.num_q_heads + h * G + n % G) * D;
+    if constexpr (kFused) {
+      // rotate the row's elements e, e + 1 with their partners e +- d/2
+      const int pos = qp ? __ldg(a.positions + q0 + n / G) : -1;
+      const bool pos_ok = pos >= 0 && pos < a.rope_max_pos;
+      const float* cs = a.rope_table + static_cast<size_t>(pos_ok ? pos : 0) * D;
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qb[nt][ks][0] = qp ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * t4)) : 0u;
-      qb[nt][ks][1] = qp ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8 + 2 * t4)) : 0u;
+      for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          const int e = 16 * ks + 8 * hb + 2 * t4;
+          const bool upper = e >= D / 2;
+          const int f = upper ? e - D / 2 : e;
+          uint32_t v = 0u;
+          if (qp && pos_ok)
+            v = rope_pair<kBf16>(__ldg(reinterpret_cast<const uint32_t*>(qp + e)),
+                                 __ldg(reinterpret_cast<const uint32_t*>(qp + (upper ? f : e + D / 2))),
+                                 __ldg(reinterpret_cast<const float4*>(cs + 2 * f)), upper);
+          qb[nt][ks][hb] = v;
+        }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qb[nt][ks][0] = qp ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * t4)) : 0u;
+        qb[nt][ks][1] = qp ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8 + 2 * t4)) : 0u;
+      }
     }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -341,7 +421,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* kmap, const CUten
   }
 }
 
-template <int D, bool kBf16>
+template <int D, bool kBf16, bool kFused>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const AttnArgs a) {
@@ -364,21 +444,28 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   if (nrows <= 8)
-    decode_body<D, kBf16, 1>(&kmap, &vmap, a, smem, s, h, split, q0, nrows, ctx, nsplit);
+    decode_body<D, kBf16, kFused, 1>(&kmap, &vmap, a, smem, s, h, split, q0, qlen, ctx, nsplit);
   else
-    decode_body<D, kBf16, 2>(&kmap, &vmap, a, smem, s, h, split, q0, nrows, ctx, nsplit);
+    decode_body<D, kBf16, kFused, 2>(&kmap, &vmap, a, smem, s, h, split, q0, qlen, ctx, nsplit);
+}
+
+template <int D, bool kBf16, bool kFused>
+cudaError_t launch_decode_f(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            cudaStream_t stream) {
+  using L = DecodeLayout<D>;
+  static std::atomic<unsigned long long> configured{0};
+  cudaError_t e = set_smem_limit_once(decode_kernel<D, kBf16, kFused>, L::kAlloc, configured);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.max_splits, a.num_kv_heads, a.num_seqs);
+  decode_kernel<D, kBf16, kFused><<<grid, kThreads, L::kAlloc, stream>>>(kmap, vmap, a);
+  return cudaGetLastError();
 }
 
 template <int D, bool kBf16>
 cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                             cudaStream_t stream) {
-  using L = DecodeLayout<D>;
-  static std::atomic<unsigned long long> configured{0};
-  cudaError_t e = set_smem_limit_once(decode_kernel<D, kBf16>, L::kAlloc, configured);
-  if (e != cudaSuccess) return e;
-  dim3 grid(a.max_splits, a.num_kv_heads, a.num_seqs);
-  decode_kernel<D, kBf16><<<grid, kThreads, L::kAlloc, stream>>>(kmap, vmap, a);
-  return cudaGetLastError();
+  return a.q_raw ? launch_decode_f<D, kBf16, true>(a, kmap, vmap, stream)
+                 : launch_decode_f<D, kBf16, false>(a, kmap, vmap, stream);
 }
 
 }  // namespace

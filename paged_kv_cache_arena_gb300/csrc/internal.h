@@ -54,6 +54,18 @@ struct AttnArgs {
   int decode_max_rows;           // query_len * group at or below this -> decode kernel
   float scale_log2;              // scale * log2(e)
   int dtype;
+  // fused decode step: when q_raw is set the decode kernel rotates the query
+  // rows itself (q_raw [T][Hq][d]) and writes the new tokens' rotated K and raw
+  // V (k_new, v_new [T][Hkv][d]) into the arena before reading it; q_rot_out
+  // (optional) receives the rotated q.
+  const void* q_raw;
+  const void* k_new;
+  const void* v_new;
+  const float* rope_table;
+  int rope_max_pos;
+  void* q_rot_out;
+  void* k_arena_w;
+  void* v_arena_w;
 };
 
 // Split-KV decode (mma.sync on staged TMA tiles); the last split of each

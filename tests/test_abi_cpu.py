@@ -156,3 +156,23 @@ def test_status_strings(lib):
     for code in range(5):
         assert lib.kshipra_status_string(code)
     assert lib.kshipra_status_string(99) == b"unknown status"
+
+
+def step_args(**over):
+    a = dict(out=FAKE, q=ctypes.c_void_p(0x30000), k=FAKE, v=FAKE, q_rot=ctypes.c_void_p(0x20000), k_arena=FAKE,
+             v_arena=FAKE, bt=FAKE, ctx=FAKE, qsl=FAKE, pos=FAKE, table=FAKE, rope_max_pos=64, num_seqs=1,
+             num_tokens=1, max_q=1, max_ctx=10, hq=4, hkv=2, d=64, bs=16, maxb=4, nb=16, scale=0.125, dtype=0,
+             ws=None, ws_bytes=0, stream=None)
+    a.update(over)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(rope_max_pos=0), 1), (dict(q=None), 1), (dict(table=None), 1), (dict(k=ctypes.c_void_p(0x10008)), 1),
+    (dict(dtype=2), 2), (dict(d=96), 2), (dict(hq=6, hkv=4), 1), (dict(q_rot=FAKE), 1),
+    # a 40-token chunk needs the two-call path, which needs q_rot
+    (dict(max_q=40, num_tokens=40, q_rot=None), 1),
+])
+def test_decode_step_validation(lib, over, code):
+    assert lib.kshipra_decode_step(*step_args(**over)) == code
+    assert lib.kshipra_last_error()

@@ -85,5 +85,14 @@ class DeviceWorkload:
         self.append_step(stream)
         self.attention(stream=stream)
 
+    def decode_step(self, q_rot=True, stream=None):
+        """Append and attention through kshipra_decode_step (one launch for
+        decode-class batches); q_rot=False passes no q_rot buffer."""
+        w = self.w
+        K.kshipra_decode_step(self.out, self.q, self.k_new, self.v_new, self.q_rot if q_rot else None, self.k_arena,
+                              self.v_arena, self.block_tables, self.context_lens, self.query_start_loc,
+                              self.positions, self.rope_table, w.max_query_len, w.max_context_len, w.scale,
+                              self.workspace, stream=stream)
+
     def out_f64(self) -> np.ndarray:
         return self.out.float().cpu().numpy().astype(np.float64)
