@@ -235,6 +235,49 @@ def gpu_launches_per_step(w, decode_max_rows=16, fused=False):
     return n
 
 
+def measure_blocks(torch, stream, pk):
+    """Secondary object: block moves.  Swap-out / swap-in of one sequence's
+    blocks (32768 tokens, 8 kv heads, head_dim 128, fp16: 128 MiB of K and V)
+    to pinned host memory over the CPU-GPU link, and the copy-on-write copy
+    of 1024 blocks inside the arena (HBM, read + write)."""
+    import paged_kv_cache_arena_gb300 as K
+    nb, hkv, bs, d = 4096, 8, 16, 128
+    k = torch.randn((nb, hkv, bs, d), device="cuda", dtype=torch.float16)
+    v = torch.randn_like(k)
+    seq = torch.randperm(nb, device="cuda")[:2048].to(torch.int32)  # 32768 tokens
+    hk = torch.empty((2048, hkv, bs, d), dtype=torch.float16, pin_memory=True)
+    hv = torch.empty_like(hk, pin_memory=True)
+    nbytes = 2 * hk.numel() * 2
+
+    def timed(fn, reps=10):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize()
+        ev = _events(torch, 2)
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for _ in range(reps):
+                fn()
+            ev[1].record(stream)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / reps
+
+    out_ms = timed(lambda: K.kshipra_blocks_swap_out(hk, hv, k, v, seq, stream=stream))
+    in_ms = timed(lambda: K.kshipra_blocks_swap_in(k, v, hk, hv, seq, stream=stream))
+    src, dst = seq[:1024].contiguous(), seq[1024:].contiguous()
+    copy_ms = timed(lambda: K.kshipra_blocks_copy(k, v, src, dst, stream=stream))
+    copy_bytes = 2 * 2 * 1024 * hkv * bs * d * 2  # K and V, read + write
+    peak = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    return {"swap_out": {"bytes": nbytes, "ms": round(out_ms, 4), "gbs": round(nbytes / out_ms / 1e6, 1),
+                         "to": "pinned host memory"},
+            "swap_in": {"bytes": nbytes, "ms": round(in_ms, 4), "gbs": round(nbytes / in_ms / 1e6, 1),
+                        "from": "pinned host memory"},
+            "cow_copy": {"blocks": 1024, "ms": round(copy_ms, 4),
+                         "roofline": {"bound": "hbm", "achieved": round(copy_bytes / copy_ms / 1e6, 1), "peak": peak,
+                                      "unit": "GB/s", "frac": round(copy_bytes / copy_ms / 1e6 / peak, 4)}}}
+
+
 def measure_prefill(torch, stream, pk):
     """Secondary object: chunked-prefill attention TFLOP/s (L2 flushed)."""
     from workloads import make_config
@@ -365,11 +408,17 @@ def gpu_arm(args, w):
     e2e_ms, h2d, d2h = time_e2e(torch, dw, e2e_steps, stream, fused=fused)
     e2e_value = world * kv * e2e_steps / (e2e_ms * 1e-3) / 1e9
     secondary = None
+    blocks = None
     if not args.no_prefill:
         try:
             secondary = measure_prefill(torch, stream, pk)
         except Exception as exc:  # reported, never silently substituted
             secondary = {"workload": "chunked-prefill", "error": str(exc)[:200]}
+    if rank == 0 and not args.no_blocks:
+        try:
+            blocks = measure_blocks(torch, stream, pk)
+        except Exception as exc:
+            blocks = {"error": str(exc)[:200]}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         secs, kv_s, _, n_s, threads = oracle_sample(w)
@@ -399,7 +448,7 @@ def gpu_arm(args, w):
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": launches, "clocks": clocks, "device_status": status,
-            "cpu_baseline": cpu, "secondary": secondary,
+            "cpu_baseline": cpu, "secondary": secondary, "blocks": blocks,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -417,6 +466,7 @@ def main():
     ap.add_argument("--step", choices=["fused", "two-call"], default="fused",
                     help="a decode step as one kshipra_decode_step launch or as append + attention calls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-blocks", action="store_true", help="skip the block-move secondary object")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

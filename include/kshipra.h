@@ -66,6 +66,7 @@ extern "C" {
 #define KSHIPRA_ERR_UNSUPPORTED 2        /* head_dim, block_size, group size or dtype not built */
 #define KSHIPRA_ERR_WORKSPACE_TOO_SMALL 3
 #define KSHIPRA_ERR_CUDA 4               /* a CUDA call failed; see kshipra_last_error() */
+#define KSHIPRA_ERR_OUT_OF_BLOCKS 5      /* the block pool has fewer free blocks than requested */
 
 /* ---- device status word bits (kshipra_device_status) ----------------- */
 #define KSHIPRA_DEV_BAD_BLOCK_ID 0x1     /* a block-table entry outside [0, num_blocks) */
@@ -135,6 +136,67 @@ int kshipra_kv_append_rope(const void* q, const void* k, const void* v, void* q_
                            const int32_t* positions, const float* rope_table, int rope_max_pos, int num_seqs,
                            int num_tokens, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                            int max_blocks_per_seq, int num_blocks, int dtype, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Block management (kshipra-3, section 1: the arena is reserved once and a
+ * LIFO free list hands blocks out and takes them back; section 3: reference
+ * counts keep shared prefix blocks alive and a block is copied before a
+ * request that diverges inside it writes it; section 5: a preempted
+ * sequence's blocks are swapped out of the arena and restored later).
+ *
+ * The pool is host state (thread-safe); it decides block ids and never
+ * touches device memory.  The move calls below do the device side.
+ */
+typedef struct kshipra_block_pool kshipra_block_pool;
+
+/* A pool over blocks 0 .. num_blocks-1, all free.  The free list starts as
+ * 0, 1, ..., num_blocks-1 and allocation takes from its end, so the first
+ * allocation returns num_blocks-1.  Errors: INVALID_ARG. */
+int kshipra_block_pool_create(int num_blocks, kshipra_block_pool** pool_out);
+void kshipra_block_pool_destroy(kshipra_block_pool* pool);
+/* Free blocks, or -1 for a NULL pool. */
+int kshipra_block_pool_num_free(kshipra_block_pool* pool);
+/* n blocks into ids_out (host array), each with reference count 1, taken
+ * from the end of the free list (the most recently released first).  All or
+ * nothing.  Errors: INVALID_ARG, OUT_OF_BLOCKS. */
+int kshipra_block_alloc(kshipra_block_pool* pool, int n, int32_t* ids_out);
+/* One more reference to each listed (allocated) block: another sequence maps
+ * it, e.g. a shared prefix.  Errors: INVALID_ARG (a block not allocated). */
+int kshipra_block_share(kshipra_block_pool* pool, const int32_t* ids, int n);
+/* Drops one reference per listed block, in order; a block whose count
+ * reaches 0 goes to the end of the free list (the next allocation reuses it).
+ * Nothing changes if any entry would drop below 0.  Errors: INVALID_ARG. */
+int kshipra_block_release(kshipra_block_pool* pool, const int32_t* ids, int n);
+/* Reference count of one block (0 = free), or -1 for a bad id / NULL pool. */
+int kshipra_block_refcount(kshipra_block_pool* pool, int id);
+/* Before writing into block *id_inout: if it is shared (count > 1), takes a
+ * fresh block for the writer, drops the writer's reference to the shared
+ * one, stores the fresh id in *id_inout and the shared id in *copy_from_out
+ * (the caller then copies the block with kshipra_blocks_copy); if it is
+ * private, *copy_from_out = -1 and nothing changes.
+ * Errors: INVALID_ARG, OUT_OF_BLOCKS. */
+int kshipra_block_make_private(kshipra_block_pool* pool, int32_t* id_inout, int32_t* copy_from_out);
+
+/* Device side, asynchronous on `stream`; arenas as for the attention calls
+ * ([num_blocks][num_kv_heads][block_size][head_dim], K and V), ids are device
+ * int32 arrays of n entries.  Ids outside the arena are reported through the
+ * device status word (KSHIPRA_DEV_BAD_BLOCK_ID) and skipped.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+/* Copies block src_ids[i] to block dst_ids[i] (all kv heads, K and V) within
+ * the arena; the two id lists must not share an id. */
+int kshipra_blocks_copy(void* k_arena, void* v_arena, const int32_t* src_ids, const int32_t* dst_ids, int n,
+                        int num_kv_heads, int block_size, int head_dim, int num_blocks, int dtype, void* stream);
+/* Gathers blocks ids[0..n) into k_out, v_out [n][num_kv_heads][block_size]
+ * [head_dim]: device memory or pinned host memory (written over the CPU-GPU
+ * link, no staging copy). */
+int kshipra_blocks_swap_out(void* k_out, void* v_out, const void* k_arena, const void* v_arena, const int32_t* ids,
+                            int n, int num_kv_heads, int block_size, int head_dim, int num_blocks, int dtype,
+                            void* stream);
+/* Scatters k_in, v_in [n][num_kv_heads][block_size][head_dim] (device or
+ * pinned host memory) into blocks ids[0..n) of the arena. */
+int kshipra_blocks_swap_in(void* k_arena, void* v_arena, const void* k_in, const void* v_in, const int32_t* ids,
+                           int n, int num_kv_heads, int block_size, int head_dim, int num_blocks, int dtype,
+                           void* stream);
 
 /*
  * Bytes of device workspace kshipra_paged_attention needs for these sizes,

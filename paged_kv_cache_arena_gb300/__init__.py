@@ -24,6 +24,7 @@ KSHIPRA_ERR_INVALID_ARG = 1
 KSHIPRA_ERR_UNSUPPORTED = 2
 KSHIPRA_ERR_WORKSPACE_TOO_SMALL = 3
 KSHIPRA_ERR_CUDA = 4
+KSHIPRA_ERR_OUT_OF_BLOCKS = 5
 
 KSHIPRA_DEV_BAD_BLOCK_ID = 0x1
 KSHIPRA_DEV_BAD_POSITION = 0x2
@@ -97,6 +98,86 @@ def kshipra_kv_append_rope(q, k, v, q_rot, k_arena, v_arena, block_tables, query
         _ptr(query_start_loc), _ptr(positions), _ptr(rope_table), rope_table.shape[0],
         query_start_loc.shape[0] - 1, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
         block_tables.shape[1], num_blocks, _dtype_code(k), _stream(stream)), "kshipra_kv_append_rope")
+
+
+class BlockPool:
+    """The library's LIFO block pool (host state; see include/kshipra.h)."""
+
+    def __init__(self, num_blocks: int):
+        lib = _lib.load()
+        h = ctypes.c_void_p(0)
+        _check(lib.kshipra_block_pool_create(num_blocks, ctypes.byref(h)), "kshipra_block_pool_create")
+        self._h = h
+        self.num_blocks = num_blocks
+
+    def close(self) -> None:
+        if self._h:
+            _lib.load().kshipra_block_pool_destroy(self._h)
+            self._h = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def num_free(self) -> int:
+        return _lib.load().kshipra_block_pool_num_free(self._h)
+
+    @staticmethod
+    def _ids(ids):
+        arr = (ctypes.c_int32 * len(ids))(*[int(i) for i in ids])
+        return arr, len(ids)
+
+    def alloc(self, n: int) -> list:
+        arr = (ctypes.c_int32 * max(n, 1))()
+        _check(_lib.load().kshipra_block_alloc(self._h, n, arr), "kshipra_block_alloc")
+        return [int(arr[i]) for i in range(n)]
+
+    def share(self, ids) -> None:
+        arr, n = self._ids(ids)
+        _check(_lib.load().kshipra_block_share(self._h, arr, n), "kshipra_block_share")
+
+    def release(self, ids) -> None:
+        arr, n = self._ids(ids)
+        _check(_lib.load().kshipra_block_release(self._h, arr, n), "kshipra_block_release")
+
+    def refcount(self, block_id: int) -> int:
+        return _lib.load().kshipra_block_refcount(self._h, int(block_id))
+
+    def make_private(self, block_id: int):
+        """(id to write into, id to copy from or -1)."""
+        bid, src = ctypes.c_int32(int(block_id)), ctypes.c_int32(0)
+        _check(_lib.load().kshipra_block_make_private(self._h, ctypes.byref(bid), ctypes.byref(src)),
+               "kshipra_block_make_private")
+        return int(bid.value), int(src.value)
+
+
+def _arena_shape(k_arena):
+    num_blocks, num_kv_heads, block_size, head_dim = k_arena.shape
+    return num_kv_heads, block_size, head_dim, num_blocks
+
+
+def kshipra_blocks_copy(k_arena, v_arena, src_ids, dst_ids, stream=None) -> None:
+    hk, bs, d, nb = _arena_shape(k_arena)
+    _check(_lib.load().kshipra_blocks_copy(_ptr(k_arena), _ptr(v_arena), _ptr(src_ids), _ptr(dst_ids),
+                                           src_ids.numel(), hk, bs, d, nb, _dtype_code(k_arena), _stream(stream)),
+           "kshipra_blocks_copy")
+
+
+def kshipra_blocks_swap_out(k_out, v_out, k_arena, v_arena, ids, stream=None) -> None:
+    hk, bs, d, nb = _arena_shape(k_arena)
+    _check(_lib.load().kshipra_blocks_swap_out(_ptr(k_out), _ptr(v_out), _ptr(k_arena), _ptr(v_arena), _ptr(ids),
+                                               ids.numel(), hk, bs, d, nb, _dtype_code(k_arena), _stream(stream)),
+           "kshipra_blocks_swap_out")
+
+
+def kshipra_blocks_swap_in(k_arena, v_arena, k_in, v_in, ids, stream=None) -> None:
+    hk, bs, d, nb = _arena_shape(k_arena)
+    _check(_lib.load().kshipra_blocks_swap_in(_ptr(k_arena), _ptr(v_arena), _ptr(k_in), _ptr(v_in), _ptr(ids),
+                                              ids.numel(), hk, bs, d, nb, _dtype_code(k_arena), _stream(stream)),
+           "kshipra_blocks_swap_in")
 
 
 def kshipra_paged_attention_workspace_size(num_seqs: int, num_tokens: int, max_context_len: int,

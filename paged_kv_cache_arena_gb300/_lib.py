@@ -18,6 +18,17 @@ EXPORTS = (
     "kshipra_kv_bytes_per_token",
     "kshipra_rope_table_build",
     "kshipra_kv_append_rope",
+    "kshipra_block_pool_create",
+    "kshipra_block_pool_destroy",
+    "kshipra_block_pool_num_free",
+    "kshipra_block_alloc",
+    "kshipra_block_share",
+    "kshipra_block_release",
+    "kshipra_block_refcount",
+    "kshipra_block_make_private",
+    "kshipra_blocks_copy",
+    "kshipra_blocks_swap_out",
+    "kshipra_blocks_swap_in",
     "kshipra_paged_attention_workspace_size",
     "kshipra_paged_attention",
     "kshipra_decode_step",
@@ -46,6 +57,19 @@ def load() -> ctypes.CDLL:
         lib.kshipra_kv_bytes_per_token.restype = SZ
         lib.kshipra_rope_table_build.argtypes = [P, I, I, D]
         lib.kshipra_kv_append_rope.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P]
+        PI32 = ctypes.POINTER(ctypes.c_int32)
+        lib.kshipra_block_pool_create.argtypes = [I, ctypes.POINTER(P)]
+        lib.kshipra_block_pool_destroy.argtypes = [P]
+        lib.kshipra_block_pool_destroy.restype = None
+        lib.kshipra_block_pool_num_free.argtypes = [P]
+        lib.kshipra_block_alloc.argtypes = [P, I, PI32]
+        lib.kshipra_block_share.argtypes = [P, PI32, I]
+        lib.kshipra_block_release.argtypes = [P, PI32, I]
+        lib.kshipra_block_refcount.argtypes = [P, I]
+        lib.kshipra_block_make_private.argtypes = [P, PI32, PI32]
+        lib.kshipra_blocks_copy.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
+        lib.kshipra_blocks_swap_out.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P]
+        lib.kshipra_blocks_swap_in.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P]
         lib.kshipra_paged_attention_workspace_size.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(SZ)]
         lib.kshipra_paged_attention.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, P, SZ, P]
         lib.kshipra_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, F, I,

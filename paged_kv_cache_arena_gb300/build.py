@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkshipra.so")
-SOURCES = ("api.cu", "append_rope.cu", "decode.cu", "prefill.cu", "prefill_pair.cu", "noalloc.cu")
+SOURCES = ("api.cu", "append_rope.cu", "decode.cu", "prefill.cu", "prefill_pair.cu", "noalloc.cu", "blocks.cu")
 HEADERS = ("common.cuh", "internal.h", "rope.cuh")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")

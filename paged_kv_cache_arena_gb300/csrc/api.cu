@@ -316,6 +316,20 @@ int attention_impl(void* out, const void* q_rot, const void* k_arena, const void
 
 }  // namespace
 
+// The same helpers for the other translation units (internal.h).
+namespace kshipra {
+void api_clear_error() { g_last_error[0] = 0; }
+int api_fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
+int api_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+cudaError_t api_status_ptr(unsigned** out) { return status_ptr(out); }
+}  // namespace kshipra
+
 // ===========================================================================
 extern "C" {
 
@@ -367,6 +381,7 @@ const char* kshipra_status_string(int code) {
     case KSHIPRA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
     case KSHIPRA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case KSHIPRA_ERR_CUDA: return "CUDA error";
+    case KSHIPRA_ERR_OUT_OF_BLOCKS: return "not enough free blocks";
     default: return "unknown status";
   }
 }

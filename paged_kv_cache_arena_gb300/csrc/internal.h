@@ -10,6 +10,13 @@
 
 namespace kshipra {
 
+// Error reporting shared by the C-ABI entry points (api.cu): set the calling
+// thread's last-error text and return the code; the device status word.
+void api_clear_error();
+int api_fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int api_cuda_fail(cudaError_t e, const char* what);
+cudaError_t api_status_ptr(unsigned** out);
+
 // Rows of (token, q head) a decode unit handles at most: query_len x group.
 constexpr int kDecodeMaxRows = 16;
 
