@@ -278,6 +278,66 @@ def measure_blocks(torch, stream, pk):
                                       "unit": "GB/s", "frac": round(copy_bytes / copy_ms / 1e6 / peak, 4)}}}
 
 
+def measure_prefix_cache():
+    """Secondary object: the radix-tree prefix cache on the host.  64 system
+    prompts of 512 tokens, each shared by 64 requests with 256 tokens of their
+    own (block_size 16: 67,584 cached blocks); times insert (request
+    finished), match (a new request: 32 shared blocks, then its own tokens)
+    and eviction of every block, leaf by leaf with cascades.  Calls go
+    straight to the C ABI with prebuilt arrays."""
+    import ctypes
+    import random
+    import time
+
+    import paged_kv_cache_arena_gb300 as K
+    from paged_kv_cache_arena_gb300 import _lib
+    lib = _lib.load()
+    bs, prompts, per_prompt, own, sys_len = 16, 64, 64, 256, 512
+    rnd = random.Random(5)
+    nblk = (sys_len + own) // bs
+    pool = K.BlockPool(prompts * per_prompt * nblk)
+    cache = K.PrefixCache(pool, bs)
+    systems = [[rnd.randrange(32000) for _ in range(sys_len)] for _ in range(prompts)]
+    arr = lambda xs: (ctypes.c_int32 * len(xs))(*xs)
+    reqs = [arr(systems[i % prompts] + [rnd.randrange(32000) for _ in range(own)])
+            for i in range(prompts * per_prompt)]
+    n = sys_len + own
+    blocks = (ctypes.c_int32 * nblk)()
+    added = ctypes.c_int(0)
+    t_ins = 0.0
+    for r in reqs:
+        lib.kshipra_block_alloc(pool._h, nblk, blocks)
+        t0 = time.perf_counter()
+        rc = lib.kshipra_prefix_cache_insert(cache._h, r, n, blocks, nblk, ctypes.byref(added))
+        t_ins += time.perf_counter() - t0
+        assert rc == 0
+        lib.kshipra_block_release(pool._h, blocks, nblk)
+    nodes = cache.num_nodes
+    probes = [arr(systems[i % prompts] + [rnd.randrange(32000) for _ in range(own)]) for i in range(2000)]
+    out, nb, nt = (ctypes.c_int32 * nblk)(), ctypes.c_int(0), ctypes.c_int(0)
+    t0 = time.perf_counter()
+    for r in probes:
+        lib.kshipra_prefix_cache_match(cache._h, r, n, out, nblk, ctypes.byref(nb), ctypes.byref(nt))
+        lib.kshipra_block_release(pool._h, out, nb.value)
+    t_match = time.perf_counter() - t0
+    assert nt.value == sys_len
+    freed = ctypes.c_int(0)
+    t0 = time.perf_counter()
+    total = 0
+    while True:
+        lib.kshipra_prefix_cache_evict(cache._h, 256, ctypes.byref(freed))
+        total += freed.value
+        if freed.value < 256:
+            break
+    t_evict = time.perf_counter() - t0
+    assert total == nodes and pool.num_free == pool.num_blocks
+    cache.close()
+    pool.close()
+    return {"nodes": nodes, "block_size": bs, "insert_us": round(t_ins / len(reqs) * 1e6, 2),
+            "match_us": round(t_match / len(probes) * 1e6, 2), "tokens_per_request": n,
+            "evict_us_per_block": round(t_evict / total * 1e6, 3), "where": "host CPU, through the C ABI"}
+
+
 def measure_prefill(torch, stream, pk):
     """Secondary object: chunked-prefill attention TFLOP/s (L2 flushed)."""
     from workloads import make_config
@@ -417,6 +477,7 @@ def gpu_arm(args, w):
     if rank == 0 and not args.no_blocks:
         try:
             blocks = measure_blocks(torch, stream, pk)
+            blocks["prefix_cache"] = measure_prefix_cache()
         except Exception as exc:
             blocks = {"error": str(exc)[:200]}
     cpu = None

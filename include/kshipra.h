@@ -198,6 +198,61 @@ int kshipra_blocks_swap_in(void* k_arena, void* v_arena, const void* k_in, const
                            int n, int num_kv_heads, int block_size, int head_dim, int num_blocks, int dtype,
                            void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Radix-tree prefix cache (kshipra-3, section 3): cached KV blocks form a tree
+ * whose edges are blocks of block_size tokens; a request walks it from the
+ * root and reuses every matching block; under memory pressure the least
+ * recently used leaf is evicted, looked up again after each eviction so that
+ * a parent left without children is considered too.
+ *
+ * Host state (thread-safe) over a block pool, which must outlive the cache.
+ * The tree holds one pool reference to each block it caches.  Recency is a
+ * logical clock that advances once per match or insert and stamps every node
+ * the call walks; ties in recency (and in the partial match below) go to the
+ * smaller block id.
+ */
+typedef struct kshipra_prefix_cache kshipra_prefix_cache;
+
+/* An empty cache over `pool` for blocks of block_size tokens.
+ * Errors: INVALID_ARG. */
+int kshipra_prefix_cache_create(kshipra_block_pool* pool, int block_size, kshipra_prefix_cache** cache_out);
+/* Drops the tree's references (blocks nobody else holds return to the pool's
+ * free list) and frees the cache. */
+void kshipra_prefix_cache_destroy(kshipra_prefix_cache* cache);
+/* The longest cached prefix of tokens[0..num_tokens): full blocks while one
+ * matches, then, if tokens remain and no full block matches them, the child
+ * sharing the longest run of leading tokens with the rest.  Writes the
+ * matched blocks to blocks_out (host array of max_blocks >=
+ * ceil(num_tokens / block_size) entries), their number to *num_blocks_out and
+ * the matched token count to *num_matched_out; the caller gets one reference
+ * to each returned block.  When *num_matched_out is not a multiple of
+ * block_size, the last block is shared and only partly the caller's: it must
+ * go through kshipra_block_make_private (and kshipra_blocks_copy) before the
+ * caller writes slot *num_matched_out % block_size.  Errors: INVALID_ARG. */
+int kshipra_prefix_cache_match(kshipra_prefix_cache* cache, const int32_t* tokens, int num_tokens,
+                               int32_t* blocks_out, int max_blocks, int* num_blocks_out, int* num_matched_out);
+/* Caches the full blocks of a computed sequence: block j of tokens (tokens
+ * [j * block_size, (j + 1) * block_size)) lives in blocks[j], for j <
+ * num_tokens / block_size (num_blocks may be larger; the partial tail is not
+ * cached).  Where the same tokens are cached already under the same parent,
+ * the cached block stays and blocks[j] is not added.  Each added block gets
+ * the tree's reference; *num_added_out (may be NULL) is their number.  All or
+ * nothing.  Errors: INVALID_ARG (too few ids, an added block not allocated,
+ * cached elsewhere already, or listed twice). */
+int kshipra_prefix_cache_insert(kshipra_prefix_cache* cache, const int32_t* tokens, int num_tokens,
+                                const int32_t* blocks, int num_blocks, int* num_added_out);
+/* Frees up to num_blocks blocks: repeatedly removes the least recently used
+ * leaf whose block only the tree holds and drops that reference.  Stops early
+ * when nothing is evictable; *num_freed_out (may be NULL) is the count.
+ * Errors: INVALID_ARG. */
+int kshipra_prefix_cache_evict(kshipra_prefix_cache* cache, int num_blocks, int* num_freed_out);
+/* Blocks evict() could free now, cascades included: nodes whose whole
+ * subtree only the tree holds (the "evictable" term of section 5's admission
+ * test, free + evictable >= reserved + needed).  -1 for a NULL cache. */
+int kshipra_prefix_cache_evictable(kshipra_prefix_cache* cache);
+/* Cached blocks (tree nodes), or -1 for a NULL cache. */
+int kshipra_prefix_cache_num_nodes(kshipra_prefix_cache* cache);
+
 /*
  * Bytes of device workspace kshipra_paged_attention needs for these sizes,
  * written to *bytes_out (host pointer).  sm_count is the number of SMs of the

@@ -180,6 +180,69 @@ def kshipra_blocks_swap_in(k_arena, v_arena, k_in, v_in, ids, stream=None) -> No
            "kshipra_blocks_swap_in")
 
 
+class PrefixCache:
+    """The library's radix-tree prefix cache over a BlockPool (host state; see
+    include/kshipra.h).  Close it before the pool."""
+
+    def __init__(self, pool: BlockPool, block_size: int):
+        h = ctypes.c_void_p(0)
+        _check(_lib.load().kshipra_prefix_cache_create(pool._h, block_size, ctypes.byref(h)),
+               "kshipra_prefix_cache_create")
+        self._h = h
+        self.pool = pool  # keeps the pool alive
+        self.block_size = block_size
+
+    def close(self) -> None:
+        if self._h:
+            _lib.load().kshipra_prefix_cache_destroy(self._h)
+            self._h = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _tokens(tokens):
+        n = len(tokens)
+        return (ctypes.c_int32 * max(n, 1))(*[int(t) for t in tokens]), n
+
+    def match(self, tokens):
+        """(blocks, matched token count); the caller holds one reference to
+        each returned block."""
+        arr, n = self._tokens(tokens)
+        cap = -(-n // self.block_size)
+        out = (ctypes.c_int32 * max(cap, 1))()
+        nb, nt = ctypes.c_int(0), ctypes.c_int(0)
+        _check(_lib.load().kshipra_prefix_cache_match(self._h, arr, n, out, cap, ctypes.byref(nb), ctypes.byref(nt)),
+               "kshipra_prefix_cache_match")
+        return [int(out[i]) for i in range(nb.value)], int(nt.value)
+
+    def insert(self, tokens, blocks) -> int:
+        """Caches the full blocks of tokens; returns how many were added."""
+        arr, n = self._tokens(tokens)
+        ids = (ctypes.c_int32 * max(len(blocks), 1))(*[int(b) for b in blocks])
+        added = ctypes.c_int(0)
+        _check(_lib.load().kshipra_prefix_cache_insert(self._h, arr, n, ids, len(blocks), ctypes.byref(added)),
+               "kshipra_prefix_cache_insert")
+        return int(added.value)
+
+    def evict(self, num_blocks: int) -> int:
+        freed = ctypes.c_int(0)
+        _check(_lib.load().kshipra_prefix_cache_evict(self._h, num_blocks, ctypes.byref(freed)),
+               "kshipra_prefix_cache_evict")
+        return int(freed.value)
+
+    @property
+    def evictable(self) -> int:
+        return _lib.load().kshipra_prefix_cache_evictable(self._h)
+
+    @property
+    def num_nodes(self) -> int:
+        return _lib.load().kshipra_prefix_cache_num_nodes(self._h)
+
+
 def kshipra_paged_attention_workspace_size(num_seqs: int, num_tokens: int, max_context_len: int,
                                            num_q_heads: int, num_kv_heads: int, head_dim: int,
                                            sm_count: int = 0) -> int:

@@ -29,6 +29,13 @@ EXPORTS = (
     "kshipra_blocks_copy",
     "kshipra_blocks_swap_out",
     "kshipra_blocks_swap_in",
+    "kshipra_prefix_cache_create",
+    "kshipra_prefix_cache_destroy",
+    "kshipra_prefix_cache_match",
+    "kshipra_prefix_cache_insert",
+    "kshipra_prefix_cache_evict",
+    "kshipra_prefix_cache_evictable",
+    "kshipra_prefix_cache_num_nodes",
     "kshipra_paged_attention_workspace_size",
     "kshipra_paged_attention",
     "kshipra_decode_step",
@@ -70,6 +77,15 @@ def load() -> ctypes.CDLL:
         lib.kshipra_blocks_copy.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
         lib.kshipra_blocks_swap_out.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P]
         lib.kshipra_blocks_swap_in.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P]
+        PI = ctypes.POINTER(I)
+        lib.kshipra_prefix_cache_create.argtypes = [P, I, ctypes.POINTER(P)]
+        lib.kshipra_prefix_cache_destroy.argtypes = [P]
+        lib.kshipra_prefix_cache_destroy.restype = None
+        lib.kshipra_prefix_cache_match.argtypes = [P, PI32, I, PI32, I, PI, PI]
+        lib.kshipra_prefix_cache_insert.argtypes = [P, PI32, I, PI32, I, PI]
+        lib.kshipra_prefix_cache_evict.argtypes = [P, I, PI]
+        lib.kshipra_prefix_cache_evictable.argtypes = [P]
+        lib.kshipra_prefix_cache_num_nodes.argtypes = [P]
         lib.kshipra_paged_attention_workspace_size.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(SZ)]
         lib.kshipra_paged_attention.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, P, SZ, P]
         lib.kshipra_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, F, I,

@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkshipra.so")
-SOURCES = ("api.cu", "append_rope.cu", "decode.cu", "prefill.cu", "prefill_pair.cu", "noalloc.cu", "blocks.cu")
+SOURCES = ("api.cu", "append_rope.cu", "decode.cu", "prefill.cu", "prefill_pair.cu", "noalloc.cu", "blocks.cu",
+           "prefix_cache.cpp")
 HEADERS = ("common.cuh", "internal.h", "rope.cuh")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
@@ -36,7 +37,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(OBJ, exist_ok=True)
     procs = []
     for src in SOURCES:
-        obj = os.path.join(OBJ, src.replace(".cu", ".o"))
+        obj = os.path.join(OBJ, os.path.splitext(src)[0] + ".o")
         cmd = [NVCC, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)

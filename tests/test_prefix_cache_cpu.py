@@ -174,3 +174,95 @@ def test_oracle_evictable_is_what_evict_frees():
         want = cache.evictable()
         assert cache.evict(10 ** 6) == want
         assert cache.evictable() == 0
+
+
+# ---- the library against the oracle
+
+def run_ops(K, seed, num_blocks=160, steps=500):
+    rnd = random.Random(seed)
+    pool_o, pool_l = LifoPool(num_blocks), K.BlockPool(num_blocks)
+    cache_o, cache_l = PrefixCache(pool_o, BS), K.PrefixCache(pool_l, BS)
+    held = []  # references the test holds (same ids on both sides)
+    prompts = [[rnd.randrange(3) for _ in range(rnd.randrange(0, 28))] for _ in range(6)]
+
+    def request_tokens():
+        base = rnd.choice(prompts)
+        return base[:rnd.randrange(len(base) + 1)] + [rnd.randrange(3) for _ in range(rnd.randrange(0, 10))]
+
+    for _ in range(steps):
+        op = rnd.choice(["match", "insert", "insert", "release", "evict", "private"])
+        if op == "match":
+            q = request_tokens()
+            got = cache_o.match(q)
+            assert cache_l.match(q) == got
+            held += got[0]
+        elif op == "insert":
+            toks = request_tokens()
+            nblk = -(-len(toks) // BS)
+            st, blocks = pool_o.alloc(nblk)
+            if st != OK:
+                with pytest.raises(K.KshipraError):
+                    pool_l.alloc(nblk)
+                continue
+            assert pool_l.alloc(nblk) == blocks
+            assert cache_l.insert(toks, blocks) == cache_o.insert(toks, blocks)[1]
+            pool_o.release(blocks)
+            pool_l.release(blocks)
+        elif op == "release" and held:
+            ids = [held.pop(rnd.randrange(len(held))) for _ in range(min(len(held), rnd.randint(1, 6)))]
+            pool_o.release(ids)
+            pool_l.release(ids)
+        elif op == "evict":
+            n = rnd.randint(0, 12)
+            assert cache_l.evict(n) == cache_o.evict(n)
+        elif op == "private" and held:
+            j = rnd.randrange(len(held))
+            st, new, src = pool_o.make_private(held[j])
+            if st == OK:
+                assert pool_l.make_private(held[j]) == (new, src)
+                held[j] = new
+            else:
+                with pytest.raises(K.KshipraError):
+                    pool_l.make_private(held[j])
+        assert cache_l.num_nodes == cache_o.num_nodes()
+        assert cache_l.evictable == cache_o.evictable()
+        assert pool_l.num_free == len(pool_o.free)
+    assert all(pool_l.refcount(i) == pool_o.refcount(i) for i in range(num_blocks))
+    cache_l.close()
+    cache_o.clear()
+    pool_l.release(held)
+    assert pool_l.num_free == num_blocks
+    pool_l.close()
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_library_cache_matches_oracle(K, seed):
+    run_ops(K, seed)
+
+
+def test_library_insert_checks_before_it_changes_anything(K):
+    pool = K.BlockPool(8)
+    cache = K.PrefixCache(pool, BS)
+    blocks = pool.alloc(2)
+    with pytest.raises(K.KshipraError):
+        cache.insert(list(range(2 * BS)), [blocks[0], 7])   # block 7 is free
+    assert cache.num_nodes == 0 and pool.refcount(blocks[0]) == 1
+    with pytest.raises(K.KshipraError):
+        cache.insert(list(range(2 * BS)), [blocks[0], blocks[0]])  # one block twice
+    with pytest.raises(K.KshipraError):
+        cache.insert(list(range(2 * BS)), blocks[:1])         # too few blocks
+    assert cache.insert(list(range(2 * BS)), blocks) == 2
+    cache.close()
+
+
+def test_library_long_chain_cascade(K):
+    # one 4096-block sequence evicted leaf by leaf, each parent in turn
+    pool = K.BlockPool(4096)
+    cache = K.PrefixCache(pool, 16)
+    blocks = pool.alloc(4096)
+    toks = list(itertools.islice(itertools.cycle(range(7)), 4096 * 16))
+    assert cache.insert(toks, blocks) == 4096
+    pool.release(blocks)
+    assert cache.evictable == 4096
+    assert cache.evict(5000) == 4096
+    assert pool.num_free == 4096 and cache.num_nodes == 0
