@@ -547,22 +547,28 @@ __device__ __forceinline__ void mask_max(uint32_t (&t)[32], int k0, int pos, boo
       if (k0 + i > pos) t[i] = __float_as_uint(kNegInf);
   }
 #pragma unroll
-  for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(t[i]));
+  for (int i = 0; i < 16; ++i) mx[i & 7] = fmax3(mx[i & 7], __uint_as_float(t[2 * i]), __uint_as_float(t[2 * i + 1]));
 }
 
 // Probabilities of 32 scores (keys 32 cc ..), their sum, and P into row r of
 // the P tile in shared memory: K-major, 128-byte swizzle (16-byte chunk c of
 // a 128-byte row segment stored at chunk c ^ (r % 8)), keys 64 g .. in
 // region g -- the layout TMA gives Q, which the MMA reads the same way.
+// Scaling, shifting and summing work on pairs (f32x2 instructions) and the
+// row maximum takes three operands at a time: the softmax warps are bound by
+// instruction issue, not by the special-function unit (moving some of the
+// exponentials to a polynomial on the FMA pipe measured slower at every
+// fraction tried).
 template <bool kBf16>
-__device__ __forceinline__ void exp_store(const uint32_t (&t)[32], float c2, float ms, float (&sums)[4],
-                                          uint32_t p_row, int cc, int r) {
+__device__ __forceinline__ void exp_store(const uint32_t (&t)[32], uint64_t c2x2, uint64_t msx2,
+                                          uint64_t (&sums)[2], uint32_t p_row, int cc, int r) {
   uint32_t pk[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float p0 = ex2(fmaf(__uint_as_float(t[2 * i]), c2, -ms));
-    const float p1 = ex2(fmaf(__uint_as_float(t[2 * i + 1]), c2, -ms));
-    sums[i & 3] += p0 + p1;
+    float x0, x1;
+    f2_unpack(f2_fma(f2_bits(t[2 * i], t[2 * i + 1]), c2x2, msx2), x0, x1);
+    const float p0 = ex2(x0), p1 = ex2(x1);
+    sums[i & 1] = f2_add(sums[i & 1], f2_pack(p0, p1));
     pk[i] = pack2<kBf16>(p0, p1);
   }
   const uint32_t seg = p_row + (cc >> 1) * Layout::kQRegion;
@@ -644,13 +650,17 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
       // the previous tile's PV MMAs must be done with each half of P_x (and
       // with O_x, which may be rescaled below) before it is written
       if (gt > 0 && !warp_wait(&b.p_free[2 * x], (gt - 1) & 1, a.status)) { ok = false; break; }
-      float sums[4] = {0.f, 0.f, 0.f, 0.f};
-      exp_store<kBf16>(t0, c2, ms, sums, p_row, 0, r);
-      exp_store<kBf16>(t1, c2, ms, sums, p_row, 1, r);
+      const uint64_t c2x2 = f2_pack(c2, c2), msx2 = f2_pack(-ms, -ms);
+      uint64_t sums[2] = {0, 0};
+      exp_store<kBf16>(t0, c2x2, msx2, sums, p_row, 0, r);
+      exp_store<kBf16>(t1, c2x2, msx2, sums, p_row, 1, r);
       if (gt > 0 && !warp_wait(&b.p_free[2 * x + 1], (gt - 1) & 1, a.status)) { ok = false; break; }
-      exp_store<kBf16>(t2, c2, ms, sums, p_row, 2, r);
-      exp_store<kBf16>(t3, c2, ms, sums, p_row, 3, r);
-      l = fmaf(l, alpha, (sums[0] + sums[1]) + (sums[2] + sums[3]));
+      exp_store<kBf16>(t2, c2x2, msx2, sums, p_row, 2, r);
+      exp_store<kBf16>(t3, c2x2, msx2, sums, p_row, 3, r);
+      float s00, s01, s10, s11;
+      f2_unpack(sums[0], s00, s01);
+      f2_unpack(sums[1], s10, s11);
+      l = fmaf(l, alpha, (s00 + s01) + (s10 + s11));
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         tc_fence_after();
 #pragma unroll
