@@ -359,6 +359,57 @@ def measure_prefill(torch, stream, pk):
             "l2": "flushed between calls (512 MiB write)"}
 
 
+def decode_class(w, decode_max_rows=16):
+    """Sequences the library sends to the decode kernel (query rows = query
+    length x group size at most decode_max_rows); the rest go to prefill."""
+    G = w.num_q_heads // w.num_kv_heads
+    return np.nonzero(w.query_lens.astype(np.int64) * G <= decode_max_rows)[0]
+
+
+def measure_workload(torch, stream, pk, name, steps=30):
+    """Secondary object for one more config: its attention call timed on the
+    launching stream (the append of its new tokens timed beside it), inputs
+    larger than L2.  Decode-class sequences are measured in KV GB/s against
+    HBM, prefill-class ones in TFLOP/s against the dense tensor peak; a
+    mixed batch runs both kernels in one call, and its fraction is the
+    larger of the two ideal times (bytes / HBM peak, flops / tensor peak)
+    over the measured call."""
+    from workloads import make_config
+    from workloads.device import DeviceWorkload
+    w = make_config(name)
+    dw = DeviceWorkload(w)
+    _, app, att = time_steps(torch, dw, steps, 5, stream)
+    att_ms, app_ms = statistics.mean(att), statistics.mean(app)
+    dec = decode_class(w)
+    pre = np.setdiff1d(np.arange(w.num_seqs), dec)
+    kv = decode_kv_bytes(w, dec)
+    flops = 0.0
+    if len(pre):
+        toks = np.concatenate([np.arange(w.query_start_loc[s], w.query_start_loc[s + 1]) for s in pre])
+        flops = 4.0 * w.head_dim * w.num_q_heads * float((w.positions[toks].astype(np.int64) + 1).sum())
+    bw, tc = pk.get("hbm_gbs"), pk.get("bf16_tflops")
+    ideal_ms = max(kv / (bw * 1e9), flops / (tc * 1e12)) * 1e3
+    out = {"workload": name, "num_seqs": w.num_seqs, "query_tokens": int(w.num_tokens),
+           "dtype": w.dtype, "block_size": w.block_size, "attention_ms_per_call": round(att_ms, 5),
+           "append_ms_per_call": round(app_ms, 5), "tokens_per_s": round(w.num_tokens / (att_ms * 1e-3), 1),
+           "decode_seqs": int(len(dec)), "decode_kv_bytes": kv, "prefill_seqs": int(len(pre)),
+           "prefill_flops": flops, "l2": "inputs larger than L2 (%.0f MB of KV read per call)" % (kv / 1e6),
+           "status": None}
+    if flops == 0.0:
+        out["roofline"] = {"bound": "hbm", "achieved": round(kv / (att_ms * 1e-3) / 1e9, 1), "peak": bw,
+                           "unit": "GB/s", "frac": round(ideal_ms / att_ms, 4), "traffic": None}
+    else:
+        out["roofline"] = {"bound": "hbm" if kv / (bw * 1e9) >= flops / (tc * 1e12) else "tensor",
+                           "achieved_gbs": round(kv / (att_ms * 1e-3) / 1e9, 1),
+                           "achieved_tflops": round(flops / (att_ms * 1e-3) / 1e12, 2),
+                           "peak_gbs": bw, "peak_tflops": tc, "ideal_ms": round(ideal_ms, 5),
+                           "frac": round(ideal_ms / att_ms, 4), "traffic": None,
+                           "frac_rule": "max(KV bytes / HBM peak, prefill flops / tensor peak) / call time"}
+    del dw
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ oracle (CPU)
 
 def oracle_sample(w, budget_s: float = 15.0):
@@ -474,6 +525,17 @@ def gpu_arm(args, w):
             secondary = measure_prefill(torch, stream, pk)
         except Exception as exc:  # reported, never silently substituted
             secondary = {"workload": "chunked-prefill", "error": str(exc)[:200]}
+    workloads = []
+    if not args.no_workloads:
+        for name in ("mixed", "long-decode"):
+            if name == w.name:
+                continue
+            try:
+                r = measure_workload(torch, stream, pk, name)
+                r["status"] = K.kshipra_device_status()
+            except Exception as exc:  # reported, never silently substituted
+                r = {"workload": name, "error": str(exc)[:200]}
+            workloads.append(r)
     if rank == 0 and not args.no_blocks:
         try:
             blocks = measure_blocks(torch, stream, pk)
@@ -509,7 +571,7 @@ def gpu_arm(args, w):
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": launches, "clocks": clocks, "device_status": status,
-            "cpu_baseline": cpu, "secondary": secondary, "blocks": blocks,
+            "cpu_baseline": cpu, "secondary": secondary, "workloads": workloads, "blocks": blocks,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -528,6 +590,7 @@ def main():
                     help="a decode step as one kshipra_decode_step launch or as append + attention calls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-blocks", action="store_true", help="skip the block-move secondary object")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the mixed and long-decode objects")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
