@@ -154,15 +154,18 @@ int check_arena(int num_blocks, int num_kv_heads, int block_size, int max_blocks
   return KSHIPRA_OK;
 }
 
-// Keys per decode split.  Aims at roughly kDecodeWaves waves of two CTAs per
-// SM for the largest batch these arguments allow, in multiples of 64 keys
-// between 256 and kDecodeMaxSplit.  Each split pays a pipeline fill and a
-// partial write, so a few long splits per sequence beat many short ones as
-// long as the grid still covers the GPU several times (on GB300, a 64 x 8
-// head batch at contexts up to 4096 is fastest near 1.5-2 K keys per split,
-// 16 x 32 K contexts near 4-8 K).
-constexpr int kDecodeWaves = 4;
-constexpr int kDecodeMaxSplit = 4096;
+// Keys per decode split.  Aims at about kDecodeWaves wave of two CTAs per SM
+// for the largest batch these arguments allow, in multiples of 64 keys
+// between 256 and kDecodeMaxSplit.  The decode kernel starts its CTAs longest
+// first, so the last wave holds the shortest work and few long splits beat
+// many short ones: every split pays its own start (a pipeline fill, the unit
+// lookup) and, when a sequence has several, a partial write and a merge.  On
+// GB300 (one wave, 8 K cap) a 64 x 8 head batch at contexts up to 4096 runs one
+// CTA per (sequence, kv head) at 0.88 of the copy bandwidth, against 0.81 at
+// two waves, 0.73 at three and 0.77 for the earlier in-order grid at four; 16
+// sequences of 32 K keys run at the copy bandwidth with four 8 K splits.
+constexpr int kDecodeWaves = 1;
+constexpr int kDecodeMaxSplit = 8192;
 
 int split_tokens_for(int num_seqs, int max_context_len, int num_kv_heads, int sm_count) {
   const int opt = g_opt_split_tokens.load();

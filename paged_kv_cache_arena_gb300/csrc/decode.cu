@@ -10,7 +10,11 @@
 //
 // Work unit (one CTA): (sequence s, kv head h, split).  All query rows that
 // share kv head h -- query_len x group rows, at most 16 -- are served from one
-// read of each K/V tile.
+// read of each K/V tile.  The CTAs take the units longest first: every full
+// split of every decode-class sequence (kv heads of one split next to each
+// other, so the heads of one arena block are read together), then the
+// sequences' shorter last splits in decreasing length, so that the last wave
+// holds the shortest work.
 //  - Each of the 4 warps owns every 4th 16-key chunk of the split and keeps a
 //    3-deep ring of shared-memory stages.  Lane 0 fills a stage with four TMA
 //    tile loads (K and V, two 64-column halves each, 128-byte swizzle)
@@ -34,6 +38,7 @@
 //    arena before it loads anything -- no other CTA reads that position -- so
 //    the step is one launch.  The rotation is the append kernel's, bit for bit.
 #include <float.h>
+#include <limits.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -421,29 +426,138 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* kmap, const CUten
   }
 }
 
+// Exclusive prefix sum of v over the CTA's threads in thread order, and the
+// CTA total.  Every thread calls it.
+__device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_tot, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int t = warp_tot[w];
+    if (w < warp) before += t;
+    total += t;
+  }
+  __syncthreads();  // warp_tot may be reused
+  return before + incl - v;
+}
+
+constexpr int kRemBuckets = 256;  // last-split lengths, in 1/256ths of a split
+
+// Context length of sequence s when it is of the decode class and its
+// lengths are consistent, else 0 (inconsistent ones reported by CTA 0).
+__device__ __forceinline__ int decode_ctx(const AttnArgs& a, int s) {
+  const int q0 = __ldg(a.query_start_loc + s);
+  const int qlen = __ldg(a.query_start_loc + s + 1) - q0;
+  if (q0 < 0 || q0 + qlen > a.num_tokens) {  // query_start_loc inconsistent with num_tokens
+    if (blockIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
+    return 0;
+  }
+  if (qlen <= 0 || qlen * a.group > a.decode_max_rows) return 0;  // empty, or handled by the prefill kernel
+  const int ctx = __ldg(a.context_lens + s);
+  if (ctx <= 0 || ctx > a.max_blocks_per_seq * a.block_size || ceil_div(ctx, a.split_tokens) > a.max_splits) {
+    if (blockIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
+    return 0;
+  }
+  return ctx;
+}
+
+// The unit of CTA blockIdx.x in the order described at the top: full splits
+// (sequence, split, kv head), then last splits by decreasing length bucket
+// (sequence order within a bucket), kv head fastest.  False when the index is
+// past the last unit.
+__device__ bool decode_unit(const AttnArgs& a, int& s_out, int& h_out, int& split_out) {
+  __shared__ int warp_tot[kWarps];
+  __shared__ int hist[kRemBuckets];
+  __shared__ int found[3];
+  const int L = a.split_tokens, H = a.num_kv_heads;
+  const int i = static_cast<int>(blockIdx.x);
+  for (int b = threadIdx.x; b < kRemBuckets; b += kThreads) hist[b] = 0;
+  if (threadIdx.x == 0) found[0] = -1;
+  __syncthreads();
+  int full_before = 0;  // full-split units of the sequences scanned so far
+  for (int b0 = 0; b0 < a.num_seqs; b0 += kThreads) {
+    const int s = b0 + static_cast<int>(threadIdx.x);
+    const int ctx = s < a.num_seqs ? decode_ctx(a, s) : 0;
+    const int nfull = ctx / L, rem = ctx - nfull * L;
+    int t;
+    const int start = full_before + H * cta_exclusive_scan(nfull, warp_tot, t);
+    if (i >= start && i < start + H * nfull) {
+      found[0] = s;
+      found[1] = (i - start) / H;
+      found[2] = (i - start) % H;
+    }
+    if (rem > 0) atomicAdd(&hist[static_cast<int>((static_cast<long long>(rem) * kRemBuckets) / L)], 1);
+    full_before += H * t;
+  }
+  __syncthreads();
+  if (found[0] >= 0) {
+    s_out = found[0];
+    split_out = found[1];
+    h_out = found[2];
+    return true;
+  }
+  // a last split: the r-th sequence with one in (bucket descending, sequence) order
+  const int r = (i - full_before) / H, h = (i - full_before) % H;
+  // buckets in descending order: thread k holds buckets 2k (after) and 2k + 1
+  static_assert(kRemBuckets == 2 * kThreads, "two buckets per thread");
+  const int b_hi = kRemBuckets - 1 - 2 * static_cast<int>(threadIdx.x), b_lo = b_hi - 1;
+  int nrem;
+  const int before = cta_exclusive_scan(hist[b_hi] + hist[b_lo], warp_tot, nrem);
+  if (r >= nrem) return false;  // past the last unit
+  __shared__ int pick[2];
+  if (r >= before && r < before + hist[b_hi]) {
+    pick[0] = b_hi;
+    pick[1] = r - before;
+  } else if (r >= before + hist[b_hi] && r < before + hist[b_hi] + hist[b_lo]) {
+    pick[0] = b_lo;
+    pick[1] = r - before - hist[b_hi];
+  }
+  __syncthreads();
+  const int bucket = pick[0], k = pick[1];
+  int seen = 0;
+  for (int b0 = 0; b0 < a.num_seqs; b0 += kThreads) {
+    const int s = b0 + static_cast<int>(threadIdx.x);
+    const int ctx = s < a.num_seqs ? decode_ctx(a, s) : 0;
+    const int rem = ctx % L;
+    const bool in = rem > 0 && static_cast<int>((static_cast<long long>(rem) * kRemBuckets) / L) == bucket;
+    int t;
+    const int idx = seen + cta_exclusive_scan(in ? 1 : 0, warp_tot, t);
+    if (in && idx == k) {
+      found[0] = s;
+      found[1] = ctx / L;
+    }
+    seen += t;
+    if (seen > k) break;
+  }
+  __syncthreads();
+  s_out = found[0];
+  split_out = found[1];
+  h_out = h;
+  return s_out >= 0;
+}
+
 template <int D, bool kBf16, bool kFused>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const AttnArgs a) {
-  const int split = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  int s, h, split;
+  if (!decode_unit(a, s, h, split)) return;
   const int q0 = __ldg(a.query_start_loc + s);
   const int qlen = __ldg(a.query_start_loc + s + 1) - q0;
-  const int nrows = qlen * a.group;
-  if (q0 < 0 || q0 + qlen > a.num_tokens) {  // query_start_loc inconsistent with num_tokens
-    if (split == 0 && h == 0 && threadIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
-    return;
-  }
-  if (qlen <= 0 || nrows > a.decode_max_rows) return;  // empty, or handled by the prefill kernel
   const int ctx = __ldg(a.context_lens + s);
   const int nsplit = ceil_div(ctx, a.split_tokens);
-  if (ctx <= 0 || ctx > a.max_blocks_per_seq * a.block_size || nsplit > a.max_splits) {
-    if (split == 0 && threadIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
-    return;
-  }
-  if (split >= nsplit) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  if (nrows <= 8)
+  if (qlen * a.group <= 8)
     decode_body<D, kBf16, kFused, 1>(&kmap, &vmap, a, smem, s, h, split, q0, qlen, ctx, nsplit);
   else
     decode_body<D, kBf16, kFused, 2>(&kmap, &vmap, a, smem, s, h, split, q0, qlen, ctx, nsplit);
@@ -456,8 +570,10 @@ cudaError_t launch_decode_f(const AttnArgs& a, const CUtensorMap& kmap, const CU
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = set_smem_limit_once(decode_kernel<D, kBf16, kFused>, L::kAlloc, configured);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.max_splits, a.num_kv_heads, a.num_seqs);
-  decode_kernel<D, kBf16, kFused><<<grid, kThreads, L::kAlloc, stream>>>(kmap, vmap, a);
+  // at most max_splits units per (sequence, kv head); CTAs past the last unit exit at once
+  const long long units = static_cast<long long>(a.max_splits) * a.num_kv_heads * a.num_seqs;
+  if (units > INT_MAX) return cudaErrorInvalidConfiguration;
+  decode_kernel<D, kBf16, kFused><<<static_cast<unsigned>(units), kThreads, L::kAlloc, stream>>>(kmap, vmap, a);
   return cudaGetLastError();
 }
 
