@@ -176,30 +176,60 @@ def time_steps(torch, dw, steps, warmup, stream, flush=None, fused=False):
     return total, app, att
 
 
-def time_e2e(torch, dw, steps, stream, fused=False):
-    """Same step through the public API from pinned host buffers: H2D of the
-    step's inputs, the step (fused or two calls), D2H of the output, every
-    step."""
-    w = dw.w
-    host = {}
-    for name in ("q", "k_new", "v_new", "block_tables", "context_lens", "query_start_loc", "positions"):
+def time_e2e(torch, dw, steps, stream, fused=False, graph=False):
+    """Same step through the public API from pinned host memory: every step
+    copies its inputs to the device (all of them packed in one pinned block,
+    one copy), runs the step (fused or two calls), copies the output back and
+    waits for it.  With graph=True those three are captured once in a CUDA
+    graph and each step replays it."""
+    names = ("q", "k_new", "v_new", "block_tables", "context_lens", "query_start_loc", "positions")
+    offs, sizes, total = {}, {}, 0
+    for name in names:
         t = getattr(dw, name)
-        host[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        sizes[name] = t.numel() * t.element_size()
+        offs[name] = total
+        total += (sizes[name] + 255) // 256 * 256
+    host = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    dev = torch.empty(total, dtype=torch.uint8, device=dw.q.device)
+    saved = {}
+    for name in names:
+        t = getattr(dw, name)
+        host[offs[name]:offs[name] + sizes[name]].copy_(t.contiguous().view(torch.uint8).reshape(-1))
+        saved[name] = t
+        setattr(dw, name, dev[offs[name]:offs[name] + sizes[name]].view(t.dtype).view(t.shape))
     out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(sizes.values())
     d2h = out_host.numel() * out_host.element_size()
-    t0, t1 = _events(torch, 2)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for _ in range(steps):
-            for name, h in host.items():
-                getattr(dw, name).copy_(h, non_blocking=True)
-            dw.decode_step(stream=stream) if fused else dw.step(stream=stream)
-            out_host.copy_(dw.out, non_blocking=True)
-            stream.synchronize()  # the caller reads the result every step
-        t1.record(stream)
-    torch.cuda.synchronize()
+    def body(st):
+        dev.copy_(host, non_blocking=True)
+        dw.decode_step(stream=st) if fused else dw.step(stream=st)
+        out_host.copy_(dw.out, non_blocking=True)
+
+    try:
+        t0, t1 = _events(torch, 2)
+        g = None
+        if graph:
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    body(stream)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                body(torch.cuda.current_stream())
+            torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(steps):
+                if g is not None:
+                    g.replay()
+                else:
+                    body(stream)
+                stream.synchronize()  # the caller reads the result every step
+            t1.record(stream)
+        torch.cuda.synchronize()
+    finally:
+        for name in names:
+            setattr(dw, name, saved[name])
     return t0.elapsed_time(t1), h2d, d2h
 
 
@@ -207,10 +237,10 @@ def time_e2e(torch, dw, steps, stream, fused=False):
 # workload, from the ncu capture summarised in
 # profiles/decode_kernel_llama-decode.md (the fused step's kernel); reported
 # only for that workload and valid while the kernel is unchanged since its
-# capture.  The attention-only kernel of the two-call step has not been
-# captured since the CTA order changed: no traffic figure for it.
+# capture (the fused step's kernel, and the attention-only kernel of the
+# two-call step).
 DECODE_TRAFFIC_LLAMA_DECODE = 592111616 + 1031936
-DECODE_TRAFFIC_LLAMA_DECODE_TWO_CALL = None
+DECODE_TRAFFIC_LLAMA_DECODE_TWO_CALL = 591848192 + 249088
 
 
 def gpu_launches_per_step(w, decode_max_rows=16, fused=False):
@@ -519,6 +549,15 @@ def gpu_arm(args, w):
     e2e_steps = min(args.steps, 300)
     e2e_ms, h2d, d2h = time_e2e(torch, dw, e2e_steps, stream, fused=fused)
     e2e_value = world * kv * e2e_steps / (e2e_ms * 1e-3) / 1e9
+    e2e_how = "plain launches every step (copy in, step, copy out)"
+    e2e_plain = round(e2e_value, 2)
+    try:
+        g_ms, _, _ = time_e2e(torch, dw, e2e_steps, stream, fused=fused, graph=True)
+        e2e_value = world * kv * e2e_steps / (g_ms * 1e-3) / 1e9
+        e2e_how = "copy in, step and copy out captured once in a CUDA graph, replayed every step"
+        graph_error = None
+    except Exception as exc:  # reported; the plain-launch figure stands
+        graph_error = str(exc)[:200]
     secondary = None
     blocks = None
     if not args.no_prefill:
@@ -570,7 +609,9 @@ def gpu_arm(args, w):
             "append_ms_per_step": round(statistics.mean(app), 5) if app else 0.0,
             "step": "one kshipra_decode_step launch" if fused else "kshipra_kv_append_rope + kshipra_paged_attention",
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "inputs": "packed in one pinned block, one host-to-device copy per step",
+                    "how": e2e_how, "plain_launches_value": e2e_plain, "graph_error": graph_error},
             "gpu_launches": launches, "clocks": clocks, "device_status": status,
             "cpu_baseline": cpu, "secondary": secondary, "workloads": workloads, "blocks": blocks,
         }
