@@ -301,9 +301,9 @@ int kshipra_paged_attention(void* out, const void* q_rot, const void* k_arena, c
  * bit for bit as the append writes them, out is the attention of the
  * rotated q -- in ONE launch when every sequence is of the decode class
  * (max_query_len x group <= KSHIPRA_OPT_DECODE_MAX_ROWS): each decode CTA
- * rotates its query rows from q in registers, and the CTA whose key split
- * holds a new token's position writes that token's K and V before it reads
- * the arena.  Otherwise the two calls run one after the other.
+ * rotates its query rows from q in registers, and in the CTA whose key split
+ * holds a new token's position the warp that reads that position writes the
+ * token's K and V first.  Otherwise the two calls run one after the other.
  *
  * q [num_tokens][num_q_heads][head_dim], k, v [num_tokens][num_kv_heads]
  * [head_dim], rope_table as for kshipra_kv_append_rope; the other arguments

@@ -33,10 +33,11 @@
 //    (atomic ticket) merges all splits.
 //  - Fused decode step (kshipra_decode_step): the kernel also does the
 //    RoPE-and-append of the step's new tokens.  Each CTA rotates its own query
-//    rows from the raw q in registers; the CTA whose split holds a new token's
-//    position writes that token's rotated K and raw V (its kv head) into the
-//    arena before it loads anything -- no other CTA reads that position -- so
-//    the step is one launch.  The rotation is the append kernel's, bit for bit.
+//    rows from the raw q in registers; in the CTA whose split holds a new
+//    token's position, the warp that loads the chunk holding it writes that
+//    token's rotated K and raw V (its kv head) into the arena before it loads
+//    anything -- no other warp or CTA reads that position -- so the step is
+//    one launch.  The rotation is the append kernel's, bit for bit.
 #include <float.h>
 #include <limits.h>
 
@@ -96,14 +97,15 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* kmap, const CUten
 
   if constexpr (kFused) {
     // the step's new tokens whose positions fall in this split: rotated K and
-    // raw V of kv head h into their arena slots, one warp per token, before
-    // this CTA loads any tile
+    // raw V of kv head h into their arena slots, each written by the warp
+    // that loads the 16-key chunk holding it, before that warp loads any
+    // tile; the other warps start at once
     constexpr int half = D / 2;
     bool wrote = false;
-    for (int i = warp; i < qlen; i += kWarps) {
+    for (int i = 0; i < qlen; ++i) {
       const int t = q0 + i;
       const int pos = __ldg(a.positions + t);
-      if (pos < tok_begin || pos >= tok_end) continue;
+      if (pos < tok_begin || pos >= tok_end || ((pos - tok_begin) / kChunk) % kWarps != warp) continue;
       if (pos >= a.rope_max_pos) {
         if (lane == 0) report(a.status, KSHIPRA_DEV_BAD_POSITION);
         continue;
@@ -123,20 +125,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* kmap, const CUten
             reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v_new) + src)[lane];
       wrote = true;
     }
-    if (wrote) fence_proxy_async_global();  // the rows above, before the tile loads below
-    __syncthreads();
-    // split 0 also stores the rotated query rows when asked to
-    if (split == 0 && a.q_rot_out != nullptr)
-      for (int n = warp; n < nrows; n += kWarps) {
-        const int t = q0 + n / a.group;
-        const int pos = __ldg(a.positions + t);
-        if (pos < 0 || pos >= a.rope_max_pos) continue;
-        const size_t row = (static_cast<size_t>(t) * a.num_q_heads + h * a.group + n % a.group) * D;
-        if (2 * lane < half)
-          rotate_two_pairs<kBf16>(static_cast<const uint16_t*>(a.q_raw) + row,
-                                  static_cast<uint16_t*>(a.q_rot_out) + row, 2 * lane, half,
-                                  a.rope_table + static_cast<size_t>(pos) * D);
-      }
+    if (wrote) fence_proxy_async_global();  // the rows above, before this warp's tile loads below
+    __syncwarp();
   }
 
   if (lane == 0) {
@@ -168,6 +158,22 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* kmap, const CUten
   int issued = 0;
   if (lane == 0) {
     for (; issued < min(kStages, my_chunks); ++issued) issue(issued);
+  }
+  if constexpr (kFused) {
+    // split 0 also stores the rotated query rows when asked to, while the
+    // first tiles are in flight
+    constexpr int half = D / 2;
+    if (split == 0 && a.q_rot_out != nullptr)
+      for (int n = warp; n < nrows; n += kWarps) {
+        const int t = q0 + n / a.group;
+        const int pos = __ldg(a.positions + t);
+        if (pos < 0 || pos >= a.rope_max_pos) continue;
+        const size_t row = (static_cast<size_t>(t) * a.num_q_heads + h * a.group + n % a.group) * D;
+        if (2 * lane < half)
+          rotate_two_pairs<kBf16>(static_cast<const uint16_t*>(a.q_raw) + row,
+                                  static_cast<uint16_t*>(a.q_rot_out) + row, 2 * lane, half,
+                                  a.rope_table + static_cast<size_t>(pos) * D);
+      }
   }
 
   // Query fragments: B operand of S^T = K q^T.  Column n of n-tile nt is
