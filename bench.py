@@ -384,6 +384,7 @@ def measure_prefill(torch, stream, pk):
     peak = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     return {"workload": "chunked-prefill", "metric": "chunked-prefill attention TFLOP/s", "unit": "TFLOP/s",
             "value": round(tflops, 2), "ms_per_call": round(att_ms, 5), "flops_per_call": flops,
+            "append_ms_per_call": round(statistics.mean(app), 5),
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(tflops / peak, 4), "traffic": None,
                          "peak_note": "fp16 dense = bf16 dense rate (measured cuBLAS bf16 burst)"},

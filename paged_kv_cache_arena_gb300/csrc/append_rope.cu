@@ -7,12 +7,15 @@
 // and section 4 (RoPE at absolute positions: a chunk after P cached tokens
 // starts at position P).
 //
-// One warp per (token, head).  The rotation (rope.cuh) is done in float32 from
-// the caller's (cos, sin) table with separately rounded products and one add,
-// then rounded once to the storage type, so the arena image is reproducible
-// bit for bit.  (float32 keeps the step off GB300's slow FP64 units.)  The
-// volume is small (num_tokens x (Hq + Hkv) x head_dim elements per call); the
-// kernel is memory-latency bound and far from the hot path's cost.
+// One CTA per token (or a few when a call has few tokens), so the token's
+// sequence, position, table row and arena block are looked up once.  The
+// token's work is cut into 16-byte units: a rotation unit rotates 8 pairs
+// (i, i + d/2) of one q or k head row (rope.cuh: float32 from the caller's
+// (cos, sin) table with separately rounded products and one add, then
+// rounded once to the storage type, so the arena image is reproducible bit
+// for bit; float32 keeps the step off GB300's slow FP64 units), a value unit
+// copies 16 bytes of one V row.  Loads and stores are 16 bytes wide and a
+// token's rows are contiguous, so the kernel streams q, k and v once.
 #include "common.cuh"
 #include "internal.h"
 #include "rope.cuh"
@@ -20,61 +23,121 @@
 namespace kshipra {
 namespace {
 
-constexpr int kAppendWarps = 4;
-constexpr int kAppendThreads = 32 * kAppendWarps;
+constexpr int kAppendThreads = 128;
 
-// One warp per (token, head): warps of blockIdx.y cover q heads first, then
-// kv heads (k rotated into the arena, v copied).  Lane i rotates pairs 2i and
-// 2i + 1; with head_dim 64 the upper half of the warp idles.
+constexpr int kUnitsInFlight = 4;  // units a thread loads before any is stored
+
+// Units of token blockIdx.x: rotation units of the q heads, then of the kv
+// heads (k into the arena), then the value units; CTA blockIdx.y of
+// gridDim.y takes every gridDim.y-th group of kAppendThreads units.  A
+// thread first loads the sources of its first kUnitsInFlight units (they
+// depend only on the token), then finds the token's sequence, position and
+// arena block, then rotates and stores: the memory round trips overlap
+// instead of following one another.
 template <bool kBf16>
 __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendArgs a) {
   const int t = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (t >= a.num_tokens) return;
+  const int pos = __ldg(a.positions + t);
+  const int D = a.head_dim, half = D / 2, groups = half / 8;
   const int nq = a.q != nullptr ? a.num_q_heads : 0;
-  const int hh = blockIdx.y * kAppendWarps + warp;  // head slot: [0, nq) q heads, then kv heads
-  if (t >= a.num_tokens || hh >= nq + a.num_kv_heads) return;
-  // sequence of token t: the last s with query_start_loc[s] <= t
-  int lo = 0, hi = a.num_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(a.query_start_loc + mid) <= t) lo = mid;
-    else hi = mid - 1;
+  const int rot_units = (nq + a.num_kv_heads) * groups;
+  const int units = rot_units + a.num_kv_heads * (D / 8);
+  const int u0 = blockIdx.y * kAppendThreads + threadIdx.x, stride = gridDim.y * kAppendThreads;
+  // source rows of unit u: q row, k row, or a 16-byte piece of a v row
+  auto src_of = [&](int u, const uint16_t*& p) -> bool {  // true: rotation unit
+    if (u < rot_units) {
+      const int hh = u / groups;
+      p = hh < nq ? static_cast<const uint16_t*>(a.q) + (static_cast<size_t>(t) * a.num_q_heads + hh) * D
+                  : static_cast<const uint16_t*>(a.k) + (static_cast<size_t>(t) * a.num_kv_heads + hh - nq) * D;
+      return true;
+    }
+    const int v = u - rot_units;
+    p = static_cast<const uint16_t*>(a.v) + (static_cast<size_t>(t) * a.num_kv_heads + v / (D / 8)) * D +
+        8 * (v % (D / 8));
+    return false;
+  };
+  uint4 lo[kUnitsInFlight], hi[kUnitsInFlight];
+#pragma unroll
+  for (int j = 0; j < kUnitsInFlight; ++j) {
+    const int u = u0 + j * stride;
+    if (u < units) {
+      const uint16_t* p;
+      if (src_of(u, p)) {
+        const int e = 8 * (u % groups);
+        lo[j] = __ldg(reinterpret_cast<const uint4*>(p + e));
+        hi[j] = __ldg(reinterpret_cast<const uint4*>(p + e + half));
+      } else {
+        lo[j] = __ldg(reinterpret_cast<const uint4*>(p));
+      }
+    }
   }
-  const int s = lo;
+  // sequence of token t: the last s with query_start_loc[s] <= t.  The
+  // entries do not decrease, so each round the CTA loads up to
+  // kAppendThreads of them evenly spaced over the remaining range and counts
+  // those <= t; two rounds cover 16 K sequences.
+  int lo_s = 0, width = a.num_seqs;
+  while (width > 1) {
+    const int step = (width + kAppendThreads - 1) / kAppendThreads;
+    const int k = static_cast<int>(threadIdx.x);
+    const bool le = k * step < width && __ldg(a.query_start_loc + lo_s + k * step) <= t;
+    const int n = __syncthreads_count(le);
+    if (n == 0) break;  // before the first sequence: caught below
+    lo_s += (n - 1) * step;
+    width = min(step, width - (n - 1) * step);
+  }
+  const int s = lo_s;
   const bool first = blockIdx.y == 0 && threadIdx.x == 0;  // reports once per token
   if (t < __ldg(a.query_start_loc + s) || t >= __ldg(a.query_start_loc + s + 1)) {  // outside every sequence
     if (first) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
     return;
   }
-  const int pos = __ldg(a.positions + t);
   if (pos < 0 || pos >= a.rope_max_pos || pos / a.block_size >= a.max_blocks_per_seq) {
     if (first) report(a.status, KSHIPRA_DEV_BAD_POSITION);
     return;
   }
-  const int D = a.head_dim, half = D / 2;
-  const float* cs = a.rope_table + static_cast<size_t>(pos) * D;  // [d/2][2] for this position
-  const int i = 2 * lane;                                           // first pair of this lane
-  if (hh < nq) {
-    const size_t row = (static_cast<size_t>(t) * a.num_q_heads + hh) * D;
-    if (i < half)
-      rotate_two_pairs<kBf16>(static_cast<const uint16_t*>(a.q) + row, static_cast<uint16_t*>(a.q_rot) + row, i,
-                              half, cs);
-    return;
-  }
-  const int h = hh - nq;
   const int blk = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + pos / a.block_size);
-  if (blk < 0 || blk >= a.num_blocks) {
-    if (lane == 0) report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
-    return;
+  const bool blk_ok = blk >= 0 && blk < a.num_blocks;
+  if (!blk_ok && first) report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
+  const float* cs = a.rope_table + static_cast<size_t>(pos) * D;  // [d/2][2] for this position
+  const size_t slot = (static_cast<size_t>(blk) * a.num_kv_heads * a.block_size + pos % a.block_size) * D;
+  // destination of unit u (nullptr: a kv unit with an invalid block)
+  auto dst_of = [&](int u) -> uint16_t* {
+    if (u < rot_units) {
+      const int hh = u / groups;
+      if (hh < nq) return static_cast<uint16_t*>(a.q_rot) + (static_cast<size_t>(t) * a.num_q_heads + hh) * D;
+      return blk_ok ? static_cast<uint16_t*>(a.k_arena) + slot + static_cast<size_t>(hh - nq) * a.block_size * D
+                    : nullptr;
+    }
+    const int v = u - rot_units;
+    return blk_ok ? static_cast<uint16_t*>(a.v_arena) + slot + static_cast<size_t>(v / (D / 8)) * a.block_size * D +
+                        8 * (v % (D / 8))
+                  : nullptr;
+  };
+#pragma unroll
+  for (int j = 0; j < kUnitsInFlight; ++j) {
+    const int u = u0 + j * stride;
+    if (u >= units) break;
+    uint16_t* d = dst_of(u);
+    if (d == nullptr) continue;
+    if (u < rot_units)
+      rotate_eight_pairs<kBf16>(lo[j], hi[j], d, 8 * (u % groups), half, cs);
+    else
+      *reinterpret_cast<uint4*>(d) = lo[j];
   }
-  const size_t src = (static_cast<size_t>(t) * a.num_kv_heads + h) * D;
-  const size_t dst = ((static_cast<size_t>(blk) * a.num_kv_heads + h) * a.block_size + pos % a.block_size) * D;
-  if (i < half)
-    rotate_two_pairs<kBf16>(static_cast<const uint16_t*>(a.k) + src, static_cast<uint16_t*>(a.k_arena) + dst, i,
-                            half, cs);
-  if (lane < D / 8)  // value row: bit copy in 16-byte pieces
-    reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.v_arena) + dst)[lane] =
-        reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) + src)[lane];
+  // shapes with more units than kUnitsInFlight per thread
+  for (int u = u0 + kUnitsInFlight * stride; u < units; u += stride) {
+    uint16_t* d = dst_of(u);
+    if (d == nullptr) continue;
+    const uint16_t* p;
+    if (src_of(u, p)) {
+      const int e = 8 * (u % groups);
+      rotate_eight_pairs<kBf16>(__ldg(reinterpret_cast<const uint4*>(p + e)),
+                           __ldg(reinterpret_cast<const uint4*>(p + e + half)), d, e, half, cs);
+    } else {
+      *reinterpret_cast<uint4*>(d) = __ldg(reinterpret_cast<const uint4*>(p));
+    }
+  }
 }
 
 }  // namespace
@@ -82,7 +145,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendArgs 
 cudaError_t launch_append_rope(const AppendArgs& a, cudaStream_t stream) {
   if (a.num_tokens == 0) return cudaSuccess;
   const int heads = (a.q != nullptr ? a.num_q_heads : 0) + a.num_kv_heads;
-  dim3 grid(a.num_tokens, (heads + kAppendWarps - 1) / kAppendWarps), block(kAppendThreads);
+  const int units = heads * (a.head_dim / 16) + a.num_kv_heads * (a.head_dim / 8);
+  // a call with few tokens (a decode step) spreads each token over several
+  // CTAs; a long one (a prefill chunk) keeps one CTA per token
+  const int per_token = a.num_tokens >= 512 ? 1 : (units + kAppendThreads - 1) / kAppendThreads;
+  dim3 grid(a.num_tokens, per_token), block(kAppendThreads);
   if (a.dtype == KSHIPRA_DTYPE_BF16)
     append_rope_kernel<true><<<grid, block, 0, stream>>>(a);
   else
