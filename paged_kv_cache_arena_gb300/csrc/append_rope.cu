@@ -25,7 +25,7 @@ namespace {
 
 constexpr int kAppendThreads = 128;
 
-constexpr int kUnitsInFlight = 4;  // units a thread loads before any is stored
+constexpr int kUnitsInFlight = 2;  // units a thread loads before any is stored
 
 // Units of token blockIdx.x: rotation units of the q heads, then of the kv
 // heads (k into the arena), then the value units; CTA blockIdx.y of
@@ -35,7 +35,7 @@ constexpr int kUnitsInFlight = 4;  // units a thread loads before any is stored
 // arena block, then rotates and stores: the memory round trips overlap
 // instead of following one another.
 template <bool kBf16>
-__global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(kAppendThreads, 16) append_rope_kernel(AppendArgs a) {
   const int t = blockIdx.x;
   if (t >= a.num_tokens) return;
   const int pos = __ldg(a.positions + t);
@@ -72,34 +72,42 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(AppendArgs 
       }
     }
   }
-  // sequence of token t: the last s with query_start_loc[s] <= t.  The
-  // entries do not decrease, so each round the CTA loads up to
-  // kAppendThreads of them evenly spaced over the remaining range and counts
-  // those <= t; two rounds cover 16 K sequences.
-  int lo_s = 0, width = a.num_seqs;
+  const bool pos_ok = pos >= 0 && pos < a.rope_max_pos && pos / a.block_size < a.max_blocks_per_seq;
+  const float* cs = a.rope_table + static_cast<size_t>(pos_ok ? pos : 0) * D;  // [d/2][2] for this position
+  if (pos_ok && static_cast<int>(threadIdx.x) * 32 < D)  // the row's 128-byte lines into L1 for the units below
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(cs + threadIdx.x * 32));
+  // sequence of token t: the last index s of query_start_loc[0..num_seqs]
+  // with an entry <= t.  The entries do not decrease, so each round the CTA
+  // loads up to kAppendThreads of them evenly spaced over the remaining
+  // range and counts those <= t; two rounds cover 16 K sequences.  t lies in
+  // sequence s unless no entry or the last one (the token count) is <= t.
+  int lo_s = 0, width = a.num_seqs + 1;
+  bool inside = true;
   while (width > 1) {
     const int step = (width + kAppendThreads - 1) / kAppendThreads;
     const int k = static_cast<int>(threadIdx.x);
     const bool le = k * step < width && __ldg(a.query_start_loc + lo_s + k * step) <= t;
     const int n = __syncthreads_count(le);
-    if (n == 0) break;  // before the first sequence: caught below
+    if (n == 0) {  // before the first sequence
+      inside = false;
+      break;
+    }
     lo_s += (n - 1) * step;
     width = min(step, width - (n - 1) * step);
   }
   const int s = lo_s;
   const bool first = blockIdx.y == 0 && threadIdx.x == 0;  // reports once per token
-  if (t < __ldg(a.query_start_loc + s) || t >= __ldg(a.query_start_loc + s + 1)) {  // outside every sequence
+  if (!inside || s >= a.num_seqs) {  // outside every sequence
     if (first) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
     return;
   }
-  if (pos < 0 || pos >= a.rope_max_pos || pos / a.block_size >= a.max_blocks_per_seq) {
+  if (!pos_ok) {
     if (first) report(a.status, KSHIPRA_DEV_BAD_POSITION);
     return;
   }
   const int blk = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + pos / a.block_size);
   const bool blk_ok = blk >= 0 && blk < a.num_blocks;
   if (!blk_ok && first) report(a.status, KSHIPRA_DEV_BAD_BLOCK_ID);
-  const float* cs = a.rope_table + static_cast<size_t>(pos) * D;  // [d/2][2] for this position
   const size_t slot = (static_cast<size_t>(blk) * a.num_kv_heads * a.block_size + pos % a.block_size) * D;
   // destination of unit u (nullptr: a kv unit with an invalid block)
   auto dst_of = [&](int u) -> uint16_t* {
