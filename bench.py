@@ -445,25 +445,26 @@ def measure_workload(torch, stream, pk, name, steps=30):
 # ------------------------------------------------------------------ oracle (CPU)
 
 def oracle_sample(w, budget_s: float = 15.0):
-    """Times the float64 oracle on whole sequences of the workload, adding
-    sequences until about `budget_s` seconds of CPU work.  Returns
-    (seconds, kv_bytes, flops, n_seqs, threads)."""
+    """Times the float64 oracle on whole sequences of the workload, taking
+    sequences in order (starting over after the last) until about
+    `budget_s` seconds of CPU work, at least one sequence.  Returns
+    (seconds, kv_bytes, flops, sequences timed, threads)."""
     import oracle
     threads = oracle.default_threads()
     qsl = w.query_start_loc
-    order = list(range(w.num_seqs))
-    done, secs = [], 0.0
-    per = None
-    while order and secs < budget_s:
-        take = 1 if per is None else max(1, min(len(order), int((budget_s - secs) / max(per, 1e-6))))
-        batch, order = order[:take], order[take:]
+    done, secs, per, nxt = [], 0.0, None, 0
+    while secs < budget_s or not done:
+        take = 1 if per is None else max(1, min(w.num_seqs, int((budget_s - secs) / max(per, 1e-6))))
+        batch = [(nxt + i) % w.num_seqs for i in range(take)]
+        nxt = (nxt + take) % w.num_seqs
         toks = np.concatenate([np.arange(qsl[s], qsl[s + 1]) for s in batch]).astype(np.int32)
         t = time.perf_counter()
         oracle.workload_attention(w, tokens=toks, nthreads=threads)
-        dt = time.perf_counter() - t
-        secs += dt
+        secs += time.perf_counter() - t
         done += batch
         per = secs / len(done)
+        if take == 1 and per is not None and secs >= budget_s:
+            break
     kv = decode_kv_bytes(w, np.array(done))
     pairs = int(sum((w.positions[qsl[s]:qsl[s + 1]].astype(np.int64) + 1).sum() for s in done))
     flops = 4.0 * w.head_dim * w.num_q_heads * pairs
@@ -476,9 +477,10 @@ def reference_arm(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+    # about two minutes of oracle work in all, at least one sequence per step
+    budget = 120.0 / max(1, args.steps + args.warmup)
     for _ in range(args.warmup):
-        oracle_sample(w, budget_s=budget / 4)
+        oracle_sample(w, budget_s=budget)
     secs = kv = 0.0
     n_seqs = threads = 0
     for _ in range(args.steps):
@@ -495,8 +497,8 @@ def reference_arm(args, w):
                        "heads": "%dq/%dkv" % (w.num_q_heads, w.num_kv_heads), "head_dim": w.head_dim,
                        "block_size": w.block_size, "l2": "n/a (CPU)"},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": "first %d of %d sequences per step (all q heads), float64 C oracle"
-                                       % (n_seqs, w.num_seqs)},
+                             "sample": "%d sequences per step, taken in order of the %d-sequence workload "
+                                       "(all q heads), float64 C oracle" % (n_seqs, w.num_seqs)},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -587,7 +589,8 @@ def gpu_arm(args, w):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         secs, kv_s, _, n_s, threads = oracle_sample(w)
         cpu = {"value": round(kv_s / secs / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": "%d of %d sequences, all q heads, float64 C oracle, %.1f s" % (n_s, w.num_seqs, secs)}
+               "sample": "%d sequences (%.1f passes over the %d-sequence workload), all q heads, float64 C "
+                         "oracle, %.1f s" % (n_s, n_s / w.num_seqs, w.num_seqs, secs)}
     launches = gpu_launches_per_step(w, fused=fused) * args.steps
     if rank == 0:
         line = {
