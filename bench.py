@@ -239,7 +239,7 @@ def time_e2e(torch, dw, steps, stream, fused=False, graph=False):
 # only for that workload and valid while the kernel is unchanged since its
 # capture (the fused step's kernel, and the attention-only kernel of the
 # two-call step).
-DECODE_TRAFFIC_LLAMA_DECODE = 592111616 + 1031936
+DECODE_TRAFFIC_LLAMA_DECODE = 592119040 + 970752
 DECODE_TRAFFIC_LLAMA_DECODE_TWO_CALL = 591848192 + 249088
 
 
