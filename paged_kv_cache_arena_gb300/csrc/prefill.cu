@@ -500,9 +500,10 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               mx[i & 7] = fmaxf(mx[i & 7], kb0 + 32 * cc + i > pos ? kNegInf : __uint_as_float(t[i]));
-          } else {
+          } else {  // three operands at a time
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(t[i]));
+            for (int i = 0; i < 16; ++i)
+              mx[i & 7] = fmax3(mx[i & 7], __uint_as_float(t[2 * i]), __uint_as_float(t[2 * i + 1]));
           }
         }
         m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
@@ -536,14 +537,22 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
             sums[i & 3] += p0 + p1;
             pk[i] = pack2<kBf16>(p0, p1);
           }
-        } else {
+        } else {  // scale-and-shift and the sums on packed pairs (f32x2)
+          const uint64_t c2x2 = f2_pack(c2, c2), msx2 = f2_pack(-ms, -ms);
+          uint64_t s2[2] = {0, 0};
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(__uint_as_float(t[2 * i]), c2, -ms));
-            const float p1 = ex2(fmaf(__uint_as_float(t[2 * i + 1]), c2, -ms));
-            sums[i & 3] += p0 + p1;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_bits(t[2 * i], t[2 * i + 1]), c2x2, msx2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            s2[i & 1] = f2_add(s2[i & 1], f2_pack(p0, p1));
             pk[i] = pack2<kBf16>(p0, p1);
           }
+          float a0, a1, b0, b1;
+          f2_unpack(s2[0], a0, a1);
+          f2_unpack(s2[1], b0, b1);
+          sums[0] += a0 + a1;
+          sums[1] += b0 + b1;
         }
         tmem_st16(s_tmem + HC * half + 16 * cc, pk);
       }
