@@ -279,6 +279,7 @@ int attention_impl(void* out, const void* q_rot, const void* k_arena, const void
   a.max_blocks_per_seq = max_blocks_per_seq; a.num_blocks = num_blocks;
   a.split_tokens = plan.split_tokens; a.max_splits = plan.max_splits;
   a.decode_max_rows = g_opt_decode_max_rows.load();
+  a.decode_ordered = num_seqs <= kDecodeOrderedMaxSeqs ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.dtype = dtype;
   if (fz) {

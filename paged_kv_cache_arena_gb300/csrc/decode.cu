@@ -14,7 +14,8 @@
 // split of every decode-class sequence (kv heads of one split next to each
 // other, so the heads of one arena block are read together), then the
 // sequences' shorter last splits in decreasing length, so that the last wave
-// holds the shortest work.
+// holds the shortest work (batches of up to 256 sequences; larger ones, many
+// waves long, take the units in index order).
 //  - Each of the 4 warps owns every 4th 16-key chunk of the split and keeps a
 //    3-deep ring of shared-memory stages.  Lane 0 fills a stage with four TMA
 //    tile loads (K and V, two 64-column halves each, 128-byte swizzle)
@@ -476,16 +477,29 @@ __device__ __forceinline__ int decode_ctx(const AttnArgs& a, int s) {
   return ctx;
 }
 
-// The unit of CTA blockIdx.x in the order described at the top: full splits
-// (sequence, split, kv head), then last splits by decreasing length bucket
-// (sequence order within a bucket), kv head fastest.  False when the index is
-// past the last unit.
+// The unit of CTA blockIdx.x.  Batches of up to kDecodeOrderedMaxSeqs
+// sequences take the order described at the top -- full splits (sequence,
+// split, kv head), then last splits by decreasing length bucket (sequence
+// order within a bucket), kv head fastest -- found by scanning the batch's
+// lengths, kThreads sequences per round.  Larger batches (many waves, a
+// small tail) take the grid in index order -- sequence, kv head, split --
+// with no scan.  False when the index names no unit.
 __device__ bool decode_unit(const AttnArgs& a, int& s_out, int& h_out, int& split_out) {
+  const int L = a.split_tokens, H = a.num_kv_heads;
+  const int i = static_cast<int>(blockIdx.x);
+  if (!a.decode_ordered) {
+    const int s = i / (H * a.max_splits), h = (i / a.max_splits) % H, split = i % a.max_splits;
+    if (s >= a.num_seqs) return false;
+    const int ctx = decode_ctx(a, s);
+    if (ctx == 0 || split >= ceil_div(ctx, L)) return false;
+    s_out = s;
+    h_out = h;
+    split_out = split;
+    return true;
+  }
   __shared__ int warp_tot[kWarps];
   __shared__ int hist[kRemBuckets];
   __shared__ int found[3];
-  const int L = a.split_tokens, H = a.num_kv_heads;
-  const int i = static_cast<int>(blockIdx.x);
   for (int b = threadIdx.x; b < kRemBuckets; b += kThreads) hist[b] = 0;
   if (threadIdx.x == 0) found[0] = -1;
   __syncthreads();

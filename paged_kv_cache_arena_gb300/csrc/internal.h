@@ -59,6 +59,7 @@ struct AttnArgs {
   int num_q_heads, num_kv_heads, group, head_dim, block_size, max_blocks_per_seq, num_blocks;
   int split_tokens, max_splits;  // decode split size (keys) and count bound
   int decode_max_rows;           // query_len * group at or below this -> decode kernel
+  int decode_ordered;            // decode CTAs take their units longest first (num_seqs <= kDecodeOrderedMaxSeqs)
   float scale_log2;              // scale * log2(e)
   int dtype;
   // fused decode step: when q_raw is set the decode kernel rotates the query
@@ -74,6 +75,11 @@ struct AttnArgs {
   void* k_arena_w;
   void* v_arena_w;
 };
+
+// Batches of at most this many sequences run their decode units longest
+// first; each decode CTA finds its unit by scanning the batch's lengths, so
+// the scan is kept to two rounds of 128 sequences.
+constexpr int kDecodeOrderedMaxSeqs = 256;
 
 // Split-KV decode (mma.sync on staged TMA tiles); the last split of each
 // (sequence, kv head) to finish merges all partials.

@@ -113,15 +113,16 @@ def test_decode_is_deterministic(clean_status):
     assert np.array_equal(a, bits_of(dw.out))
 
 
+@pytest.mark.parametrize("copies", [14, 110])
 @pytest.mark.parametrize("split", [None, 64])
-def test_full_and_last_splits_in_one_batch(clean_status, split):
+def test_full_and_last_splits_in_one_batch(clean_status, split, copies):
     # the decode CTAs take every full split first, then the shorter last splits
     # by decreasing length: contexts that are whole multiples of the split
     # (no last split), contexts one key past a multiple (a one-key last split),
     # equal contexts (equal last splits, kept in sequence order) and a
-    # one-key context, across more than 128 sequences (two rounds of the
-    # CTA's scan over the batch)
-    ctx = [64, 128, 192, 65, 129, 1, 100, 100, 63, 256] * 14
+    # one-key context; 140 sequences take that order, 1100 (more than the
+    # ordered lookup holds) the grid's index order
+    ctx = [64, 128, 192, 65, 129, 1, 100, 100, 63, 256] * copies
     w = custom(37, Hq=8, Hkv=2, prefix=[c - 1 for c in ctx], qlen=[1] * len(ctx))
     dw = run(w, split=split)
     assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype, "full and last splits")
