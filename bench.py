@@ -503,6 +503,22 @@ def reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(torch, dist, x: float, device) -> float:
+    """The largest x over all ranks (every rank gets it): the job's timed
+    region ends when its slowest replica does."""
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: float, steps: int, total_ms: float) -> float:
+    """Whole-job rate in giga-units per second: every rank processes
+    units_per_rank per step (weak scaling), over the max-over-ranks time."""
+    return world * units_per_rank * steps / (total_ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ main
 
 def gpu_arm(args, w):
@@ -541,12 +557,10 @@ def gpu_arm(args, w):
         barrier()
     clocks = clk.summary()
     if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(torch, dist, total_ms, "cuda")
     status = K.kshipra_device_status()
     ms_step = total_ms / args.steps
-    value = world * kv * args.steps / (total_ms * 1e-3) / 1e9
+    value = job_throughput(world, kv, args.steps, total_ms)
     att_ms = statistics.mean(att)
     achieved = kv / (att_ms * 1e-3) / 1e9
     e2e_steps = min(args.steps, 300)
