@@ -274,8 +274,9 @@ int kshipra_paged_attention_workspace_size(int num_seqs, int num_tokens, int max
  * Accumulation is float32; out is rounded once to dtype.
  *
  * Sequences with query_len x group <= KSHIPRA_OPT_DECODE_MAX_ROWS run on a
- * split-KV decode kernel (partial results in `workspace`, then a combine
- * pass); the others on a tcgen05 tensor-core chunked-prefill kernel with
+ * split-KV decode kernel (partial results of sequences cut into several
+ * splits in `workspace`, merged inside the same kernel by the split that
+ * finishes last); the others on a tcgen05 tensor-core chunked-prefill kernel with
  * fully masked key tiles skipped.  The split is decided on the device, so
  * one call may mix both kinds.
  *
