@@ -176,3 +176,37 @@ def step_args(**over):
 def test_decode_step_validation(lib, over, code):
     assert lib.kshipra_decode_step(*step_args(**over)) == code
     assert lib.kshipra_last_error()
+
+
+# block moves (copy-on-write copy, swap-out, swap-in): host checks before any launch
+_P = ctypes.c_void_p(0x100000)  # 16-byte aligned stand-in; no call below reaches the device
+
+
+def _move_calls(lib, n=1, heads=8, bs=16, d=128, nblocks=64, dtype=0, ids=_P, ka=_P, va=_P, kb=_P, vb=_P):
+    return {
+        "copy": lambda: lib.kshipra_blocks_copy(ka, va, ids, ids, n, heads, bs, d, nblocks, dtype, None),
+        "swap_out": lambda: lib.kshipra_blocks_swap_out(kb, vb, ka, va, ids, n, heads, bs, d, nblocks, dtype, None),
+        "swap_in": lambda: lib.kshipra_blocks_swap_in(ka, va, kb, vb, ids, n, heads, bs, d, nblocks, dtype, None),
+    }
+
+
+@pytest.mark.parametrize("call", ["copy", "swap_out", "swap_in"])
+@pytest.mark.parametrize("over, code, why", [
+    (dict(n=-1), 1, "negative block count"),
+    (dict(heads=0), 1, "bad arena shape"),
+    (dict(nblocks=0), 1, "bad arena shape"),
+    (dict(d=96), 2, "head_dim 96"),
+    (dict(bs=8), 2, "block_size 8"),
+    (dict(dtype=7), 2, "dtype 7"),
+    (dict(ids=None), 1, "NULL"),                              # id list missing for n > 0
+    (dict(ka=None), 1, "a required pointer is NULL"),         # an arena missing
+    (dict(va=ctypes.c_void_p(0x100008)), 1, "16-byte aligned"),
+])
+def test_block_move_validation(lib, call, over, code, why):
+    assert _move_calls(lib, **over)[call]() == code
+    assert why in lib.kshipra_last_error().decode()  # rejected by that check, before any CUDA call
+
+
+@pytest.mark.parametrize("call", ["copy", "swap_out", "swap_in"])
+def test_block_move_of_nothing_is_a_noop(lib, call):
+    assert _move_calls(lib, n=0, ids=None, ka=None, va=None, kb=None, vb=None)[call]() == 0
