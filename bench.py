@@ -471,14 +471,17 @@ def oracle_sample(w, budget_s: float = 15.0):
     return secs, kv, flops, len(done), threads
 
 
+REFERENCE_BUDGET_S = 120.0  # seconds of oracle work in a whole reference run
+
+
 def reference_arm(args, w):
     """The oracle as the reference implementation: each step is a bounded
     sample of the same workload, timed on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    # about two minutes of oracle work in all, at least one sequence per step
-    budget = 120.0 / max(1, args.steps + args.warmup)
+    # about REFERENCE_BUDGET_S of oracle work in all, at least one sequence per step
+    budget = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)
     for _ in range(args.warmup):
         oracle_sample(w, budget_s=budget)
     secs = kv = 0.0

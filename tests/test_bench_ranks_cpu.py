@@ -53,3 +53,28 @@ def test_reference_arm_prints_only_on_rank_zero(monkeypatch, capsys):
 
     bench.reference_arm(Args(), make_config("tiny"))  # returns at once, no oracle work
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_keeps_the_contract(monkeypatch, capsys):
+    # the oracle timed as the reference arm: one JSON line with the keys the
+    # driver reads, on the decode workload's metric and config
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    from workloads import make_config
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setattr(bench, "REFERENCE_BUDGET_S", 0.5)
+
+    class Args:
+        steps, warmup, gpus = 2, 1, 1
+
+    bench.reference_arm(Args(), make_config("llama-decode"))
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["metric"] == "decode KV-read GB/s" and line["unit"] == "GB/s"
+    assert line["config"]["workload"] == "llama-decode" and line["value"] > 0 and line["higher_is_better"]
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
