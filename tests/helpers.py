@@ -42,3 +42,15 @@ def random_decode(seed, S, lo, hi, **kw):
     rng = np.random.Generator(np.random.PCG64(seed + 1000))
     ctx = rng.integers(lo, hi, size=S, endpoint=True)
     return custom(seed, prefix=ctx - 1, qlen=np.ones(S, dtype=np.int64), **kw)
+
+
+def one_sequence(w, s):
+    """Sequence s of workload w on its own: same arena size and block ids,
+    same q, k and v rows."""
+    import dataclasses
+    qsl, ks = w.query_start_loc, w.kv_start
+    return dataclasses.replace(
+        w, name="%s[%d]" % (w.name, s), prefix_lens=w.prefix_lens[s:s + 1].copy(),
+        query_lens=w.query_lens[s:s + 1].copy(), block_tables=w.block_tables[s:s + 1].copy(),
+        q=w.q[qsl[s]:qsl[s + 1]].copy(), k_all=w.k_all[ks[s]:ks[s + 1]].copy(),
+        v_all=w.v_all[ks[s]:ks[s + 1]].copy(), shared_prefix_len=0, shared_seqs=())

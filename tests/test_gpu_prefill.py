@@ -133,3 +133,18 @@ def test_long_work_list_planned_on_its_own(clean_status):
     w = custom(36, Hq=8, Hkv=2, prefix=prefix, qlen=[5] * S)
     dw = run(w)
     assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype, "1030 chunks")
+
+
+def test_batched_equals_sequential(clean_status):
+    # kshipra-2 section 2's batching check ("batched output equals
+    # sequential"): every (sequence, kv head) is computed the same way whatever
+    # else is in the batch, so at a fixed split size each sequence's output is
+    # bit-identical run alone or batched -- prefill chunks and decode rows
+    # mixed, several splits per decode sequence
+    from helpers import one_sequence
+    w = custom(50, prefix=[0, 130, 300, 700, 45, 2000], qlen=[200, 1, 77, 1, 3, 1])
+    batched = bits_of(run(w, split=64).out)
+    qsl = w.query_start_loc
+    for s in range(w.num_seqs):
+        alone = bits_of(run(one_sequence(w, s), split=64).out)
+        assert np.array_equal(batched[qsl[s]:qsl[s + 1]], alone), "sequence %d" % s
