@@ -39,21 +39,27 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def open_library(path: str):
+    """ctypes handle of a compiled oracle (``liboracle.so``, or a copy built
+    from a modified source by the tests that plant mistakes in it)."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I, L, D = ctypes.c_int, ctypes.c_long, ctypes.c_double
+    lib.oracle_rope_table.argtypes = [P, I, I, D]
+    lib.oracle_rope_rows.argtypes = [P, P, P, L, I, I, D, I]
+    lib.oracle_arena_image.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, D, I]
+    lib.oracle_attention.argtypes = [P, P, I, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, D, I, I]
+    lib.oracle_decode_bits.argtypes = [P, P, L, I]
+    lib.oracle_encode_bits.argtypes = [P, P, L, I]
+    lib.oracle_default_threads.restype = I
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            P = ctypes.c_void_p
-            I, L, D = ctypes.c_int, ctypes.c_long, ctypes.c_double
-            lib.oracle_rope_table.argtypes = [P, I, I, D]
-            lib.oracle_rope_rows.argtypes = [P, P, P, L, I, I, D, I]
-            lib.oracle_arena_image.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I, D, I]
-            lib.oracle_attention.argtypes = [P, P, I, P, P, P, P, P, P, P, I, I, I, I, I, D, D, I, I]
-            lib.oracle_decode_bits.argtypes = [P, P, L, I]
-            lib.oracle_encode_bits.argtypes = [P, P, L, I]
-            lib.oracle_default_threads.restype = I
-            _lib = lib
+            _lib = open_library(build())
     return _lib
 
 
@@ -124,10 +130,16 @@ def arena_image(k_arena, v_arena, k_rows, v_rows, query_start_loc, positions, bl
 
 
 def attention(q, k_all, v_all, kv_start, query_start_loc, positions, context_lens, num_kv_heads: int,
-              theta: float, scale: float, dtype, tokens=None, nthreads: int = 0) -> np.ndarray:
+              theta: float, scale: float, dtype, tokens=None, nthreads: int = 0, block_tables=None,
+              block_size: int = 0, num_blocks: int = 0) -> np.ndarray:
     """Dense masked softmax attention in float64.
 
-    Returns ``[len(tokens), Hq, d]`` (all tokens when ``tokens`` is None).
+    With ``block_tables`` the keys and values are written into the oracle's
+    own arena of ``num_blocks`` blocks of ``block_size`` slots through the
+    tables and gathered back through them (a gathered NaN, an aliased slot or
+    a block id outside the arena raises); without, they are read in logical
+    order.  Returns ``[len(tokens), Hq, d]`` (all tokens when ``tokens`` is
+    None).
     """
     qq = _c(q, np.uint16)
     T, Hq, d = qq.shape
@@ -135,21 +147,33 @@ def attention(q, k_all, v_all, kv_start, query_start_loc, positions, context_len
     ks = _c(kv_start, np.int64)
     qsl, pos, ctx = _c(query_start_loc, np.int32), _c(positions, np.int32), _c(context_lens, np.int32)
     toks = None if tokens is None else _c(tokens, np.int32)
+    bt = None if block_tables is None else _c(block_tables, np.int32)
     n_out = T if toks is None else len(toks)
     out = np.zeros((n_out, Hq, d), dtype=np.float64)
     rc = _load().oracle_attention(_p(out), _p(toks) if toks is not None else ctypes.c_void_p(0), n_out, _p(qq),
-                                  _p(ka), _p(va), _p(ks), _p(qsl), _p(pos), _p(ctx), len(qsl) - 1, T, Hq,
-                                  num_kv_heads, d, float(theta), float(scale), DTYPE[dtype], int(nthreads))
+                                  _p(ka), _p(va), _p(ks), _p(qsl), _p(pos), _p(ctx),
+                                  _p(bt) if bt is not None else ctypes.c_void_p(0),
+                                  bt.shape[1] if bt is not None else 0, int(block_size), int(num_blocks),
+                                  len(qsl) - 1, T, Hq, num_kv_heads, d, float(theta), float(scale), DTYPE[dtype],
+                                  int(nthreads))
     if rc:
-        raise ValueError("oracle_attention failed (%d)" % rc)
+        raise ValueError("oracle_attention failed (%d: %s)" % (rc, _ATTN_ERRORS.get(rc, "?")))
     return out
+
+
+_ATTN_ERRORS = {1: "bad shape", 2: "block id outside the arena", 3: "out of memory",
+                4: "position outside the context", 5: "two different rows written to one arena slot",
+                6: "a NaN was gathered"}
 
 
 # ---- conveniences over a generated workload (duck-typed) -----------------
 
-def workload_attention(w, tokens=None, nthreads: int = 0) -> np.ndarray:
+def workload_attention(w, tokens=None, nthreads: int = 0, gather: bool = True) -> np.ndarray:
+    """Attention of a workload's query tokens, keys and values through the
+    oracle's own block arena (``gather=False``: in logical order)."""
+    bt = dict(block_tables=w.block_tables, block_size=w.block_size, num_blocks=w.num_blocks) if gather else {}
     return attention(w.q, w.k_all, w.v_all, w.kv_start, w.query_start_loc, w.positions, w.context_lens,
-                     w.num_kv_heads, w.theta, w.scale, w.dtype, tokens=tokens, nthreads=nthreads)
+                     w.num_kv_heads, w.theta, w.scale, w.dtype, tokens=tokens, nthreads=nthreads, **bt)
 
 
 def workload_arena(w, sentinel: int, include_prefix: bool = True, include_step: bool = True):

@@ -14,6 +14,13 @@
  *    softmax is stated to equal dense masked attention.  The oracle computes
  *    that dense definition directly: explicit mask, row maximum, exponentials,
  *    normalisation, weighted sum of V, all in float64.
+ *  - The attention reads its keys and values the way section 1 lays them out:
+ *    every raw K/V row is first written into the oracle's own arena (every
+ *    slot starts as a NaN pattern) at slot j % bs of physical block
+ *    block_tables[s][j / bs], then gathered back through the same tables; a
+ *    gathered NaN, a block id outside the arena, or a slot written twice with
+ *    different bits (two sequences' rows aliased) is an error.  A second route
+ *    reads the rows in logical order, for cross-checking the first.
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *  - RoPE pairs element i with i + d/2 ("rotate half"), frequency
@@ -242,6 +249,12 @@ typedef struct {
     const int32_t* qsl;          /* [S+1] query_start_loc */
     const int32_t* positions;    /* [T] */
     const int32_t* context_lens; /* [S] */
+    /* the oracle's own arena [num_blocks][Hkv][bs][d] (raw bits) and the
+     * tables that address it; NULL arena: read k_all/v_all in logical order */
+    const uint16_t* arena_k;
+    const uint16_t* arena_v;
+    const int32_t* block_tables; /* [S][max_blocks] */
+    int max_blocks, bs, num_blocks;
     int S, Hq, Hkv, d, dtype;
     double theta, scale;
     int* task_seq;               /* tasks are (sequence, kv head) pairs */
@@ -270,12 +283,26 @@ static void attention_task(attn_job* J, int s, int g) {
         free(K); free(V); free(w); free(visible);
         return;
     }
-    /* rotated keys and values of this (sequence, kv head), every position */
+    /* rotated keys and values of this (sequence, kv head), every position:
+     * gathered from the arena through the block table (section 1), or read
+     * in logical order on the cross-check route */
     for (long j = 0; j < ctx; ++j) {
-        size_t src = ((size_t)(J->kv_start[s] + j) * Hkv + g) * d;
-        for (int i = 0; i < d; ++i) x[i] = to_f64(J->k_all[src + i], J->dtype);
+        const uint16_t *kr, *vr;
+        if (J->arena_k) {
+            int blk = J->block_tables[(size_t)s * J->max_blocks + j / J->bs];
+            size_t slot = (((size_t)blk * Hkv + g) * J->bs + (size_t)(j % J->bs)) * d;
+            kr = J->arena_k + slot;
+            vr = J->arena_v + slot;
+        } else {
+            size_t src = ((size_t)(J->kv_start[s] + j) * Hkv + g) * d;
+            kr = J->k_all + src;
+            vr = J->v_all + src;
+        }
+        for (int i = 0; i < d; ++i) x[i] = to_f64(kr[i], J->dtype);
+        for (int i = 0; i < d; ++i) V[(size_t)j * d + i] = to_f64(vr[i], J->dtype);
+        for (int i = 0; i < d; ++i)
+            if (isnan(x[i]) || isnan(V[(size_t)j * d + i])) J->status = 6; /* a NaN was gathered */
         rope_row(x, K + (size_t)j * d, j, d, J->theta);
-        for (int i = 0; i < d; ++i) V[(size_t)j * d + i] = to_f64(J->v_all[src + i], J->dtype);
     }
     for (int r = 0; r < J->n_out; ++r) {
         int t = J->out_tokens[r];
@@ -323,6 +350,46 @@ static void* attention_worker(void* arg) {
     return NULL;
 }
 
+/* The arena every slot of which starts as the NaN pattern ARENA_EMPTY
+ * (a NaN in binary16 and in bfloat16); the raw K/V rows of each listed
+ * sequence are written to slot j % bs of block block_tables[s][j / bs]
+ * (section 1).  Returns 0; 2 a block id outside [0, num_blocks) or a
+ * logical block past the table; 5 a slot written twice with different bits
+ * (rows of different positions or sequences aliased); 3 out of memory. */
+#define ARENA_EMPTY 0x7FC1u
+
+static int arena_fill(uint16_t** ak, uint16_t** av, const char* want, const uint16_t* k_all, const uint16_t* v_all,
+                      const int64_t* kv_start, const int32_t* context_lens, const int32_t* block_tables,
+                      int max_blocks, int num_seqs, int num_blocks, int Hkv, int bs, int d) {
+    size_t n = (size_t)num_blocks * Hkv * bs * d;
+    uint16_t* K = (uint16_t*)malloc(sizeof(uint16_t) * (n ? n : 1));
+    uint16_t* V = (uint16_t*)malloc(sizeof(uint16_t) * (n ? n : 1));
+    if (!K || !V) { free(K); free(V); return 3; }
+    for (size_t i = 0; i < n; ++i) K[i] = V[i] = (uint16_t)ARENA_EMPTY;
+    *ak = K;
+    *av = V;
+    for (int s = 0; s < num_seqs; ++s) {
+        if (!want[s]) continue;
+        for (long j = 0; j < context_lens[s]; ++j) {
+            if (j / bs >= max_blocks) return 2;
+            int blk = block_tables[(size_t)s * max_blocks + j / bs];
+            if (blk < 0 || blk >= num_blocks) return 2;
+            for (int h = 0; h < Hkv; ++h) {
+                size_t src = ((size_t)(kv_start[s] + j) * Hkv + h) * d;
+                size_t dst = (((size_t)blk * Hkv + h) * bs + (size_t)(j % bs)) * d;
+                size_t row = (size_t)d * sizeof(uint16_t);
+                if (K[dst] != (uint16_t)ARENA_EMPTY) { /* written before: must hold the same row */
+                    if (memcmp(K + dst, k_all + src, row) || memcmp(V + dst, v_all + src, row)) return 5;
+                    continue;
+                }
+                memcpy(K + dst, k_all + src, row);
+                memcpy(V + dst, v_all + src, row);
+            }
+        }
+    }
+    return 0;
+}
+
 int oracle_default_threads(void) {
     long n = sysconf(_SC_NPROCESSORS_ONLN);
     return n > 0 ? (int)n : 1;
@@ -330,13 +397,19 @@ int oracle_default_threads(void) {
 
 /* out[r][h][:] = softmax-weighted sum of V for query token out_tokens[r]
  * (all T tokens when out_tokens is NULL, then n_out = T), every q head.
- * Returns 0; 1 bad shape; 3 out of memory; 4 a position outside [0, ctx). */
+ * With block_tables given, keys and values go through the oracle's own
+ * arena of num_blocks blocks of bs slots (written, then gathered, through
+ * the tables); with block_tables NULL they are read in logical order.
+ * Returns 0; 1 bad shape; 2 a block id outside the arena; 3 out of memory;
+ * 4 a position outside [0, ctx); 5 aliased arena slots; 6 a NaN gathered. */
 int oracle_attention(double* out, const int32_t* out_tokens, int n_out, const uint16_t* q,
                      const uint16_t* k_all, const uint16_t* v_all, const int64_t* kv_start,
                      const int32_t* query_start_loc, const int32_t* positions, const int32_t* context_lens,
+                     const int32_t* block_tables, int max_blocks, int block_size, int num_blocks,
                      int num_seqs, int num_tokens, int Hq, int Hkv, int d, double theta, double scale,
                      int dtype, int nthreads) {
     if (Hkv <= 0 || Hq % Hkv || d <= 0 || (d & 1) || d > 1024 || num_seqs < 0) return 1;
+    if (block_tables && (max_blocks <= 0 || block_size <= 0 || num_blocks <= 0)) return 1;
     int32_t* all = NULL;
     if (!out_tokens) {
         all = (int32_t*)malloc(sizeof(int32_t) * (size_t)(num_tokens > 0 ? num_tokens : 1));
@@ -369,6 +442,17 @@ int oracle_attention(double* out, const int32_t* out_tokens, int n_out, const ui
                 J.task_head[J.n_tasks] = g;
                 J.n_tasks++;
             }
+    uint16_t *ak = NULL, *av = NULL;
+    if (block_tables) {
+        int rc = arena_fill(&ak, &av, want, k_all, v_all, kv_start, context_lens, block_tables, max_blocks,
+                            num_seqs, num_blocks, Hkv, block_size, d);
+        if (rc) {
+            free(ak); free(av); free(want); free(J.task_seq); free(J.task_head); free(all);
+            return rc;
+        }
+        J.arena_k = ak; J.arena_v = av; J.block_tables = block_tables;
+        J.max_blocks = max_blocks; J.bs = block_size; J.num_blocks = num_blocks;
+    }
     if (nthreads <= 0) nthreads = oracle_default_threads();
     if (nthreads > J.n_tasks) nthreads = J.n_tasks > 0 ? J.n_tasks : 1;
     pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
@@ -378,6 +462,6 @@ int oracle_attention(double* out, const int32_t* out_tokens, int n_out, const ui
         else break;
     attention_worker(&J);
     for (int i = 1; i <= started; ++i) pthread_join(th[i], NULL);
-    free(th); free(want); free(J.task_seq); free(J.task_head); free(all);
+    free(th); free(want); free(J.task_seq); free(J.task_head); free(all); free(ak); free(av);
     return J.status;
 }

@@ -189,6 +189,84 @@ def test_stored_rotation_is_one_rounding_from_exact(oracle_mod, dtype):
             assert e <= unit * abs(exact[i]) + 4 * 2.0 ** -24 * (abs(x[t, i]) + abs(x[t, (i + d // 2) % d])) + 1e-30
 
 
+def _f32_rotation_restated(rows, pos, theta, dtype, mutate=None):
+    """The stored rotation written out again with numpy float32 scalars in
+    arrays (no code shared with the oracle): cos and sin of the float64
+    angle position * theta^(-2i/d) from Python's math module, each rounded
+    once to float32; y_i = x_i c - x_{i+d/2} s and y_{i+d/2} = x_{i+d/2} c +
+    x_i s with every product and the add/subtract rounded to float32 (numpy
+    never fuses them); then one rounding, nearest with ties to even, to the
+    storage type.  ``mutate`` plants one plausible mistake: "fma" (the
+    subtract/add fused with its first product, one rounding), "cos32" (the
+    angle and its cos/sin evaluated in float32), "f64" (the whole rotation
+    in float64, rounded once to storage)."""
+    import math
+    n, H, d = rows.shape
+    h = d // 2
+    if dtype == "f16":
+        x = rows.view(np.float16).astype(np.float32)
+    else:
+        x = (rows.astype(np.uint32) << 16).view(np.float32)
+    cs = {}
+    for p in np.unique(pos):
+        c = np.empty(h, np.float64)
+        s = np.empty(h, np.float64)
+        for i in range(h):
+            ang = float(p) * theta ** (-2.0 * i / d)
+            c[i], s[i] = math.cos(ang), math.sin(ang)
+        if mutate == "cos32":
+            ang32 = (np.float32(p) * (np.float32(theta) ** (np.float32(-2.0) * np.arange(h, dtype=np.float32)
+                                                            / np.float32(d)))).astype(np.float32)
+            cs[int(p)] = (np.cos(ang32).astype(np.float32), np.sin(ang32).astype(np.float32))
+        elif mutate == "f64":
+            cs[int(p)] = (c, s)
+        else:
+            cs[int(p)] = (c.astype(np.float32), s.astype(np.float32))
+    C = np.stack([cs[int(p)][0] for p in pos])[:, None, :]
+    S = np.stack([cs[int(p)][1] for p in pos])[:, None, :]
+    a, b = x[..., :h], x[..., h:]
+    if mutate == "f64":
+        a, b = a.astype(np.float64), b.astype(np.float64)
+        y = np.concatenate([a * C - b * S, b * C + a * S], axis=-1)
+    elif mutate == "fma":
+        a64, b64, C64, S64 = (v.astype(np.float64) for v in (a, b, C, S))
+        lo = (a64 * C64 - (b * S).astype(np.float64)).astype(np.float32)  # a*c exact in float64
+        hi = (b64 * C64 + (a * S).astype(np.float64)).astype(np.float32)
+        y = np.concatenate([lo, hi], axis=-1)
+    else:
+        y = np.concatenate([a * C - b * S, b * C + a * S], axis=-1)
+        assert y.dtype == np.float32
+    if dtype == "f16":
+        return y.astype(np.float16).view(np.uint16)
+    u = y.astype(np.float32).view(np.uint32) if mutate != "f64" else None
+    if mutate == "f64":  # one rounding of the float64 value straight to bfloat16
+        from oracle import f64_to_bits
+        return f64_to_bits(y, "bf16")
+    return ((u + (((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF))) >> np.uint32(16)).astype(np.uint16)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("d,theta", [(64, 1.0e4), (128, 5.0e5)])
+def test_stored_rotation_bit_for_bit(oracle_mod, dtype, d, theta):
+    # 100,000 rows at positions up to 32767 (4000 distinct, the ends included)
+    rng = np.random.default_rng(17 + d)
+    n = 100000
+    draw = rng.standard_normal((n, 1, d)).astype(np.float32) * np.float32(3.0)
+    if dtype == "f16":
+        rows = draw.astype(np.float16).view(np.uint16)
+    else:
+        u = draw.view(np.uint32)
+        rows = ((u + (((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF))) >> np.uint32(16)).astype(np.uint16)
+    distinct = np.concatenate([[0, 1, 32766, 32767], rng.integers(0, 32768, 3996)])
+    pos = distinct[rng.integers(0, len(distinct), n)].astype(np.int32)
+    got = oracle_mod.rope_rows(rows, pos, theta, dtype)
+    want = _f32_rotation_restated(rows, pos, theta, dtype)
+    assert np.array_equal(got, want)
+    # the pin is sharp: each planted mistake changes some of these rows
+    for mutate in ("fma", "cos32", "f64"):
+        assert not np.array_equal(got, _f32_rotation_restated(rows, pos, theta, dtype, mutate)), mutate
+
+
 def _rot_f64(x, p, tab_row):
     h = len(x) // 2
     c, s = tab_row[:, 0], tab_row[:, 1]
@@ -303,16 +381,20 @@ def test_split_combine_equals_dense(oracle_mod):
 
 
 def test_decode_equals_last_row_of_prefill(oracle_mod):
+    # the oracle's decode of each sequence's last token equals the last row of
+    # the brute-force prefill over the same sequence (kshipra-3 section 4:
+    # a query at position p sees keys 0..p whichever call it comes in)
     w = small(31, 8, 2, 32, 4, "f16", [19, 4], [9, 6], spare=2)
-    full = oracle_mod.workload_attention(w)
-    # the same sequences, everything but the last token already cached
+    full = brute.attention(w.q.tolist(), w.k_all.tolist(), w.v_all.tolist(), w.prefix_lens.tolist(),
+                           w.query_lens.tolist(), w.block_tables.tolist(), w.block_size, w.num_kv_heads, w.theta,
+                           w.scale, w.dtype)
     w1 = small(31, 8, 2, 32, 4, "f16", [19, 4], [9, 6], spare=2)
     w1.prefix_lens = w.prefix_lens + w.query_lens - 1
     w1.query_lens = np.ones_like(w.query_lens)
     last = w.query_start_loc[1:] - 1
     w1.q = w.q[last]
     dec = oracle_mod.workload_attention(w1)
-    assert np.max(np.abs(dec - full[last])) == 0.0
+    assert np.max(np.abs(dec - np.array(full)[last])) < 1e-12
 
 
 def test_first_token_attends_only_to_itself(oracle_mod):
@@ -347,6 +429,42 @@ def test_dominant_key_selects_its_value(oracle_mod):
     for h in range(2):
         best = int(np.argmax(kr[:13, 0] @ qr[0, h]))
         assert np.max(np.abs(out[0, h] - v[best, 0])) < 1e-9
+
+
+@pytest.mark.parametrize("make", MICRO)
+def test_arena_route_equals_logical_route(oracle_mod, make):
+    # keys and values written into the oracle's arena and gathered back
+    # through the block tables are the rows read in logical order (kshipra-3
+    # section 1), shared prefix blocks included
+    w = make()
+    assert np.array_equal(oracle_mod.workload_attention(w), oracle_mod.workload_attention(w, gather=False))
+
+
+def test_arena_route_rejects_aliased_blocks(oracle_mod):
+    # two sequences whose tables name one physical block for different rows
+    w = small(61, 4, 2, 8, 4, "f16", [9, 14], [3, 1], spare=3)
+    w.block_tables[1, 0] = w.block_tables[0, 0]
+    with pytest.raises(ValueError, match="two different rows"):
+        oracle_mod.workload_attention(w)
+    # the same aliasing inside one sequence
+    w = small(62, 4, 2, 8, 4, "f16", [9], [3], spare=3)
+    w.block_tables[0, 1] = w.block_tables[0, 0]
+    with pytest.raises(ValueError, match="two different rows"):
+        oracle_mod.workload_attention(w)
+
+
+def test_arena_route_rejects_ids_outside_the_arena(oracle_mod):
+    w = small(63, 4, 2, 8, 4, "f16", [9, 14], [3, 1], spare=3)
+    w.block_tables[0, 2] = w.num_blocks
+    with pytest.raises(ValueError, match="outside the arena"):
+        oracle_mod.workload_attention(w)
+
+
+def test_arena_route_reports_a_gathered_nan(oracle_mod):
+    w = small(64, 4, 2, 8, 4, "f16", [9, 14], [3, 1], spare=3)
+    w.k_all[5, 1, 3] = 0x7E00  # a NaN row in the arena
+    with pytest.raises(ValueError, match="NaN"):
+        oracle_mod.workload_attention(w)
 
 
 # ---------------------------------------------------------------- arena
