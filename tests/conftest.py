@@ -40,3 +40,19 @@ def clean_status(gpu):
     gpu.kshipra_set_option(gpu.KSHIPRA_OPT_SPLIT_TOKENS, 0)
     gpu.kshipra_set_option(gpu.KSHIPRA_OPT_DECODE_MAX_ROWS, 16)
     assert code == 0, "device status word 0x%x" % code
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Achieved errors of the full-size workloads against the oracle."""
+    try:
+        from helpers import RECORDED, TOL
+    except ImportError:
+        return
+    rows = [r for r in RECORDED if r[0].startswith("full ")]
+    if not rows:
+        return
+    terminalreporter.write_sep("-", "attention vs float64 oracle, full-size workloads (every output row)")
+    for what, dtype, max_abs, max_rel, n in rows:
+        atol, rtol = TOL[dtype]
+        terminalreporter.write_line("%-40s %-4s rows %5d  max abs %.3e (tol %.1e)  max rel %.3e (tol %.1e)" % (
+            what, dtype, n, max_abs, atol, max_rel, rtol))

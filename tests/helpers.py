@@ -20,9 +20,15 @@ def errors(got: np.ndarray, ref: np.ndarray):
     return max_abs, max_abs / max(denom, 1e-30)
 
 
+# (what, dtype, max abs, max rel, rows compared) of every check, printed at the
+# end of the session by conftest.py
+RECORDED = []
+
+
 def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "attention"):
     assert np.all(np.isfinite(got)), "%s: non-finite output" % what
     max_abs, max_rel = errors(got, ref)
+    RECORDED.append((what, dtype, max_abs, max_rel, int(got.shape[0]) if got.ndim else 1))
     atol, rtol = TOL[dtype]
     assert max_abs <= atol and max_rel <= rtol, "%s: max abs %.3g (tol %g), max rel %.3g (tol %g)" % (
         what, max_abs, atol, max_rel, rtol)

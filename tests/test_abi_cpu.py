@@ -70,53 +70,99 @@ def test_rope_table_rejects_bad_arguments(lib):
     assert lib.kshipra_rope_table_build(p, 0, 4, 1e4) == 0
 
 
-FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+class Mem:
+    """Real, zero-filled, 256-byte aligned memory for every pointer argument
+    of the validation tests: device memory when a GPU is present, so that a
+    host check that stopped rejecting would launch on valid buffers (zero
+    lengths, block ids and positions) rather than on invented addresses;
+    host memory otherwise (without a device no kernel can launch).  Each
+    name gets its own buffer of ``SIZE`` bytes, kept for the module."""
+
+    SIZE = 1 << 20
+
+    def __init__(self):
+        try:
+            import torch
+            self.torch = torch if torch.cuda.is_available() else None
+        except ImportError:
+            self.torch = None
+        self.bufs = {}
+
+    def __call__(self, name, offset=0):
+        if name not in self.bufs:
+            if self.torch is not None:
+                t = self.torch.zeros(self.SIZE, dtype=self.torch.uint8, device="cuda")
+                base = t.data_ptr()
+            else:
+                t = np.zeros(self.SIZE + 256, dtype=np.uint8)
+                base = (t.ctypes.data + 255) // 256 * 256
+            self.bufs[name] = (t, base)
+        return ctypes.c_void_p(self.bufs[name][1] + offset)
 
 
-def append_args(**over):
-    a = dict(q=FAKE, k=FAKE, v=FAKE, q_rot=FAKE, k_arena=FAKE, v_arena=FAKE, bt=FAKE, qsl=FAKE, pos=FAKE,
-             table=FAKE, rope_max_pos=64, num_seqs=1, num_tokens=1, hq=4, hkv=2, d=64, bs=16, maxb=4, nb=16,
-             dtype=0, stream=None)
+@pytest.fixture(scope="module")
+def mem():
+    return Mem()
+
+
+class Ptr:
+    """A pointer argument resolved against ``mem`` when the call is made:
+    buffer ``name`` plus ``offset`` bytes."""
+
+    def __init__(self, name, offset=0):
+        self.name, self.offset = name, offset
+
+
+def _resolve(mem, values):
+    return [mem(v.name, v.offset) if isinstance(v, Ptr) else v for v in values]
+
+
+def append_args(mem, **over):
+    a = dict(q=Ptr("q"), k=Ptr("k"), v=Ptr("v"), q_rot=Ptr("q_rot"), k_arena=Ptr("k_arena"),
+             v_arena=Ptr("v_arena"), bt=Ptr("bt"), qsl=Ptr("qsl"), pos=Ptr("pos"), table=Ptr("table"),
+             rope_max_pos=64, num_seqs=1, num_tokens=1, hq=4, hkv=2, d=64, bs=16, maxb=4, nb=16, dtype=0,
+             stream=None)
     a.update(over)
-    return list(a.values())
+    return _resolve(mem, a.values())
 
 
 @pytest.mark.parametrize("over,code", [
     (dict(num_seqs=-1), 1), (dict(num_tokens=-1), 1), (dict(num_seqs=0), 1), (dict(hq=5), 1), (dict(hkv=0), 1),
     (dict(hq=48, hkv=2), 2), (dict(d=96), 2), (dict(bs=8), 2), (dict(dtype=2), 2), (dict(nb=0), 1),
     (dict(maxb=0), 1), (dict(q=None), 1), (dict(k=None), 1), (dict(bt=None), 1), (dict(table=None), 1),
-    (dict(rope_max_pos=0), 1), (dict(k_arena=ctypes.c_void_p(0x10008)), 1),
+    (dict(rope_max_pos=0), 1), (dict(k_arena=Ptr("k_arena", 8)), 1),
     (dict(nb=1 << 26, hkv=8, hq=8), 2),
 ])
-def test_append_validation(lib, over, code):
-    assert lib.kshipra_kv_append_rope(*append_args(**over)) == code
+def test_append_validation(lib, mem, over, code):
+    assert lib.kshipra_kv_append_rope(*append_args(mem, **over)) == code
     assert lib.kshipra_last_error()
 
 
-def test_append_with_no_tokens_is_a_noop(lib):
-    assert lib.kshipra_kv_append_rope(*append_args(num_tokens=0, num_seqs=0)) == 0
+def test_append_with_no_tokens_is_a_noop(lib, mem):
+    assert lib.kshipra_kv_append_rope(*append_args(mem, num_tokens=0, num_seqs=0)) == 0
 
 
-def attn_args(**over):
-    a = dict(out=FAKE, q_rot=ctypes.c_void_p(0x20000), k_arena=FAKE, v_arena=FAKE, bt=FAKE, ctx=FAKE, qsl=FAKE,
-             pos=FAKE, num_seqs=1, num_tokens=1, max_q=1, max_ctx=10, hq=4, hkv=2, d=64, bs=16, maxb=4, nb=16,
-             scale=0.125, dtype=0, ws=None, ws_bytes=0, stream=None)
+def attn_args(mem, **over):
+    a = dict(out=Ptr("out"), q_rot=Ptr("q_rot"), k_arena=Ptr("k_arena"), v_arena=Ptr("v_arena"), bt=Ptr("bt"),
+             ctx=Ptr("ctx"), qsl=Ptr("qsl"), pos=Ptr("pos"), num_seqs=1, num_tokens=1, max_q=1, max_ctx=10, hq=4,
+             hkv=2, d=64, bs=16, maxb=4, nb=16, scale=0.125, dtype=0, ws=Ptr("ws"), ws_bytes=Mem.SIZE,
+             stream=None)
     a.update(over)
-    return list(a.values())
+    return _resolve(mem, a.values())
 
 
 @pytest.mark.parametrize("over,code", [
     (dict(num_seqs=-1), 1), (dict(num_seqs=0), 1), (dict(max_ctx=0), 1), (dict(max_q=0), 1),
     (dict(max_ctx=65), 1), (dict(hq=6, hkv=4), 1), (dict(hq=24, hkv=1), 2), (dict(d=256), 2), (dict(bs=64), 2),
     (dict(dtype=-1), 2), (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(out=None), 1),
-    (dict(ctx=None), 1), (dict(q_rot=FAKE), 1), (dict(v_arena=ctypes.c_void_p(0x10004)), 1),
+    (dict(ctx=None), 1), (dict(q_rot=Ptr("out")), 1), (dict(v_arena=Ptr("v_arena", 4)), 1),
 ])
-def test_attention_validation(lib, over, code):
-    assert lib.kshipra_paged_attention(*attn_args(**over)) == code
+def test_attention_validation(lib, mem, over, code):
+    assert lib.kshipra_paged_attention(*attn_args(mem, **over)) == code
 
 
-def test_attention_with_no_tokens_is_a_noop(lib):
-    assert lib.kshipra_paged_attention(*attn_args(num_tokens=0, num_seqs=0)) == 0
+def test_attention_with_no_tokens_is_a_noop(lib, mem):
+    assert lib.kshipra_paged_attention(*attn_args(mem, num_tokens=0, num_seqs=0)) == 0
 
 
 def test_workspace_size_host_only(lib):
@@ -152,39 +198,70 @@ def test_options_validation(lib):
     assert lib.kshipra_set_option(1, 16) == 0
 
 
+def test_options_belong_to_the_calling_thread(lib):
+    # two host threads with different split sizes, querying workspace sizes
+    # at the same time, each see only their own setting (ctypes drops the
+    # interpreter lock during the calls)
+    import threading
+    import paged_kv_cache_arena_gb300 as K
+    want = {}
+    for split in (256, 1024):
+        K.kshipra_set_option(K.KSHIPRA_OPT_SPLIT_TOKENS, split)
+        want[split] = K.kshipra_paged_attention_workspace_size(16, 16, 32768, 32, 8, 128, sm_count=152)
+    K.kshipra_set_option(K.KSHIPRA_OPT_SPLIT_TOKENS, 0)
+    auto = K.kshipra_paged_attention_workspace_size(16, 16, 32768, 32, 8, 128, sm_count=152)
+    assert len({want[256], want[1024], auto}) == 3
+    seen, start = {}, threading.Barrier(2)
+
+    def worker(split):
+        K.kshipra_set_option(K.KSHIPRA_OPT_SPLIT_TOKENS, split)
+        start.wait()
+        seen[split] = {K.kshipra_paged_attention_workspace_size(16, 16, 32768, 32, 8, 128, sm_count=152)
+                       for _ in range(2000)}
+
+    threads = [threading.Thread(target=worker, args=(s_,)) for s_ in (256, 1024)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert seen == {256: {want[256]}, 1024: {want[1024]}}
+    # this thread's setting was never touched by the workers
+    assert K.kshipra_paged_attention_workspace_size(16, 16, 32768, 32, 8, 128, sm_count=152) == auto
+
+
 def test_status_strings(lib):
     for code in range(5):
         assert lib.kshipra_status_string(code)
     assert lib.kshipra_status_string(99) == b"unknown status"
 
 
-def step_args(**over):
-    a = dict(out=FAKE, q=ctypes.c_void_p(0x30000), k=FAKE, v=FAKE, q_rot=ctypes.c_void_p(0x20000), k_arena=FAKE,
-             v_arena=FAKE, bt=FAKE, ctx=FAKE, qsl=FAKE, pos=FAKE, table=FAKE, rope_max_pos=64, num_seqs=1,
-             num_tokens=1, max_q=1, max_ctx=10, hq=4, hkv=2, d=64, bs=16, maxb=4, nb=16, scale=0.125, dtype=0,
-             ws=None, ws_bytes=0, stream=None)
+def step_args(mem, **over):
+    a = dict(out=Ptr("out"), q=Ptr("q"), k=Ptr("k"), v=Ptr("v"), q_rot=Ptr("q_rot"), k_arena=Ptr("k_arena"),
+             v_arena=Ptr("v_arena"), bt=Ptr("bt"), ctx=Ptr("ctx"), qsl=Ptr("qsl"), pos=Ptr("pos"),
+             table=Ptr("table"), rope_max_pos=64, num_seqs=1, num_tokens=1, max_q=1, max_ctx=10, hq=4, hkv=2, d=64,
+             bs=16, maxb=4, nb=16, scale=0.125, dtype=0, ws=Ptr("ws"), ws_bytes=Mem.SIZE, stream=None)
     a.update(over)
-    return list(a.values())
+    return _resolve(mem, a.values())
 
 
 @pytest.mark.parametrize("over,code", [
-    (dict(rope_max_pos=0), 1), (dict(q=None), 1), (dict(table=None), 1), (dict(k=ctypes.c_void_p(0x10008)), 1),
-    (dict(dtype=2), 2), (dict(d=96), 2), (dict(hq=6, hkv=4), 1), (dict(q_rot=FAKE), 1),
+    (dict(rope_max_pos=0), 1), (dict(q=None), 1), (dict(table=None), 1), (dict(k=Ptr("k", 8)), 1),
+    (dict(dtype=2), 2), (dict(d=96), 2), (dict(hq=6, hkv=4), 1), (dict(q_rot=Ptr("out")), 1),
     # a 40-token chunk needs the two-call path, which needs q_rot
     (dict(max_q=40, num_tokens=40, q_rot=None), 1),
 ])
-def test_decode_step_validation(lib, over, code):
-    assert lib.kshipra_decode_step(*step_args(**over)) == code
+def test_decode_step_validation(lib, mem, over, code):
+    assert lib.kshipra_decode_step(*step_args(mem, **over)) == code
     assert lib.kshipra_last_error()
 
 
 # block moves (copy-on-write copy, swap-out, swap-in): host checks before any launch
-_P = ctypes.c_void_p(0x100000)  # 16-byte aligned stand-in; no call below reaches the device
 
-
-def _move_calls(lib, n=1, heads=8, bs=16, d=128, nblocks=64, dtype=0, ids=_P, ka=_P, va=_P, kb=_P, vb=_P):
+def _move_calls(lib, mem, n=1, heads=8, bs=16, d=128, nblocks=64, dtype=0, ids=Ptr("ids"), ka=Ptr("k_arena"),
+                va=Ptr("v_arena"), kb=Ptr("k_dense"), vb=Ptr("v_dense"), dst=Ptr("dst_ids")):
+    ids, ka, va, kb, vb, dst = _resolve(mem, [ids, ka, va, kb, vb, dst])
     return {
-        "copy": lambda: lib.kshipra_blocks_copy(ka, va, ids, ids, n, heads, bs, d, nblocks, dtype, None),
+        "copy": lambda: lib.kshipra_blocks_copy(ka, va, ids, dst, n, heads, bs, d, nblocks, dtype, None),
         "swap_out": lambda: lib.kshipra_blocks_swap_out(kb, vb, ka, va, ids, n, heads, bs, d, nblocks, dtype, None),
         "swap_in": lambda: lib.kshipra_blocks_swap_in(ka, va, kb, vb, ids, n, heads, bs, d, nblocks, dtype, None),
     }
@@ -200,13 +277,13 @@ def _move_calls(lib, n=1, heads=8, bs=16, d=128, nblocks=64, dtype=0, ids=_P, ka
     (dict(dtype=7), 2, "dtype 7"),
     (dict(ids=None), 1, "NULL"),                              # id list missing for n > 0
     (dict(ka=None), 1, "a required pointer is NULL"),         # an arena missing
-    (dict(va=ctypes.c_void_p(0x100008)), 1, "16-byte aligned"),
+    (dict(va=Ptr("v_arena", 8)), 1, "16-byte aligned"),
 ])
-def test_block_move_validation(lib, call, over, code, why):
-    assert _move_calls(lib, **over)[call]() == code
+def test_block_move_validation(lib, mem, call, over, code, why):
+    assert _move_calls(lib, mem, **over)[call]() == code
     assert why in lib.kshipra_last_error().decode()  # rejected by that check, before any CUDA call
 
 
 @pytest.mark.parametrize("call", ["copy", "swap_out", "swap_in"])
-def test_block_move_of_nothing_is_a_noop(lib, call):
-    assert _move_calls(lib, n=0, ids=None, ka=None, va=None, kb=None, vb=None)[call]() == 0
+def test_block_move_of_nothing_is_a_noop(lib, mem, call):
+    assert _move_calls(lib, mem, n=0, ids=None, ka=None, va=None, kb=None, vb=None, dst=None)[call]() == 0

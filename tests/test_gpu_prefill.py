@@ -102,26 +102,15 @@ def test_first_chunk_token_sees_only_itself(clean_status):
         assert np.array_equal(got[:, g], v0)
 
 
-def test_full_chunked_prefill_sampled(clean_status):
-    w = make_config("chunked-prefill")
+@pytest.mark.parametrize("name", ["tiny", "chunked-prefill", "mixed"])
+def test_full_config_every_row(clean_status, name):
+    # every output row of the full-size workloads against the oracle (the
+    # chunks, the decodes of the mixed step, the shared prefix blocks)
+    w = make_config(name)
     dw = run(w)
     got = dw.out_f64()
     assert np.all(np.isfinite(got))
-    rng = np.random.default_rng(2)
-    toks = np.sort(np.concatenate([rng.choice(w.num_tokens, 60, replace=False), [0, 511, 512, 2047]])).astype(np.int32)
-    assert_close(got[toks], oracle.workload_attention(w, tokens=toks), w.dtype, "chunked-prefill sample")
-
-
-def test_full_mixed_step_sampled(clean_status):
-    w = make_config("mixed")
-    dw = run(w)
-    got = dw.out_f64()
-    assert np.all(np.isfinite(got))
-    rng = np.random.default_rng(3)
-    chunk_tokens = rng.choice(int(w.query_start_loc[8]), 40, replace=False)
-    dec_tokens = rng.choice(np.arange(int(w.query_start_loc[8]), w.num_tokens), 40, replace=False)
-    toks = np.sort(np.concatenate([chunk_tokens, dec_tokens])).astype(np.int32)
-    assert_close(got[toks], oracle.workload_attention(w, tokens=toks), w.dtype, "mixed sample")
+    assert_close(got, oracle.workload_attention(w), w.dtype, "full %s (attention)" % name)
 
 
 def test_long_work_list_planned_on_its_own(clean_status):

@@ -63,7 +63,7 @@ def serve(K, pool, cache, rows, tokens, k_arena, v_arena, rope):
                               D ** -0.5, ws)
     torch.cuda.synchronize()
     ref = oracle.attention(q[m:], k, v, np.array([0]), np.array(qsl), np.array(pos), np.array(ctx), HKV, THETA,
-                           D ** -0.5, "f16")
+                           D ** -0.5, "f16", block_tables=np.array([blocks]), block_size=BS, num_blocks=NB)
     err = np.abs(out.float().cpu().numpy().astype(np.float64) - ref).max()
     assert err <= 2e-3, (m, err)
     cache.insert(tokens, blocks)

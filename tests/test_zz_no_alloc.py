@@ -63,11 +63,20 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(clean_status):
     K = clean_status
     lib = K._lib.load()
     K.kshipra_set_option(K.KSHIPRA_OPT_SPLIT_TOKENS, 64)
-    need = K.kshipra_paged_attention_workspace_size(64, 64, 4096, 32, 8, 128)
+    S, ctx, hq, hkv, d, bs = 64, 4096, 32, 8, 128, 16
+    need = K.kshipra_paged_attention_workspace_size(S, S, ctx, hq, hkv, d)
     assert need > 16 << 20
-    fake = ctypes.c_void_p(0x100000)
-    rc = lib.kshipra_paged_attention_noalloc(fake, ctypes.c_void_p(0x200000), fake, fake, fake, fake, fake, fake,
-                                             64, 64, 1, 4096, 32, 8, 128, 16, 256, 100000, ctypes.c_float(0.088),
-                                             0, None)
+    # real, zero-filled buffers of the sizes the call names: were the size
+    # check ever to let this call through, its kernels would read and write
+    # valid memory only (zero lengths, block 0)
+    nb, maxb = 256, ctx // bs
+    dev = lambda shape, dt: torch.zeros(shape, dtype=dt, device="cuda")
+    out, q_rot = dev((S, hq, d), torch.float16), dev((S, hq, d), torch.float16)
+    ka, va = dev((nb, hkv, bs, d), torch.float16), dev((nb, hkv, bs, d), torch.float16)
+    bt, ctx_lens = dev((S, maxb), torch.int32), dev((S,), torch.int32)
+    qsl, pos = dev((S + 1,), torch.int32), dev((S,), torch.int32)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    rc = lib.kshipra_paged_attention_noalloc(p(out), p(q_rot), p(ka), p(va), p(bt), p(ctx_lens), p(qsl), p(pos), S, S,
+                                             1, ctx, hq, hkv, d, bs, maxb, nb, ctypes.c_float(d ** -0.5), 0, None)
     assert rc == K.KSHIPRA_ERR_WORKSPACE_TOO_SMALL
     assert b"workspace" in lib.kshipra_last_error()
