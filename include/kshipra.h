@@ -78,8 +78,12 @@ extern "C" {
 #define KSHIPRA_DTYPE_BF16 1
 
 /* ---- options (kshipra_set_option) ------------------------------------ */
+/* Options belong to the calling host thread (each thread starts with the
+ * defaults): a call uses the settings of the thread that makes it, so a
+ * workspace size queried on a thread fits that thread's later calls, and
+ * threads that set different values never affect each other. */
 /* Keys per decode split (0 = automatic).  Nonzero values must be multiples
- * of 64.  Process-wide; affects the workspace size. */
+ * of 64.  Affects the workspace size. */
 #define KSHIPRA_OPT_SPLIT_TOKENS 0
 /* A sequence whose query_len x group size is at most this many rows runs on
  * the split-KV decode kernel, all others on the tensor-core prefill kernel.
@@ -183,7 +187,10 @@ int kshipra_block_make_private(kshipra_block_pool* pool, int32_t* id_inout, int3
  * device status word (KSHIPRA_DEV_BAD_BLOCK_ID) and skipped.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 /* Copies block src_ids[i] to block dst_ids[i] (all kv heads, K and V) within
- * the arena; the two id lists must not share an id. */
+ * the arena.  The copies run in no fixed order, so the destination ids must
+ * be distinct and no destination may also be a source (a block copied while
+ * it is overwritten gives either content); the lists are device memory and
+ * are not checked. */
 int kshipra_blocks_copy(void* k_arena, void* v_arena, const int32_t* src_ids, const int32_t* dst_ids, int n,
                         int num_kv_heads, int block_size, int head_dim, int num_blocks, int dtype, void* stream);
 /* Gathers blocks ids[0..n) into k_out, v_out [n][num_kv_heads][block_size]
@@ -335,8 +342,12 @@ int kshipra_decode_step(void* out, const void* q, const void* k, const void* v, 
  * a fixed scratch array of KSHIPRA_NOALLOC_SCRATCH_BYTES bytes inside the
  * library, which every GPU that loads the library holds until the process
  * exits.  Sizes whose partials need more than that are rejected with
- * KSHIPRA_ERR_WORKSPACE_TOO_SMALL before anything is launched (query the need
- * with kshipra_paged_attention_workspace_size).  The first call on a device
+ * KSHIPRA_ERR_WORKSPACE_TOO_SMALL before anything is launched.  The need
+ * depends on the calling thread's KSHIPRA_OPT_SPLIT_TOKENS (shorter splits,
+ * more partials) and on the device's SM count (the automatic split size
+ * follows it), so a size that fits under one setting or device may not fit
+ * under another: query it with kshipra_paged_attention_workspace_size on the
+ * same thread, with the same option and the device's SM count.  The first call on a device
  * looks up the scratch address on that device (make it before any stream
  * capture).  All calls share the one array: calls that overlap on the GPU
  * (different streams, or several host threads) race and corrupt each
@@ -360,7 +371,8 @@ int kshipra_paged_attention_noalloc(void* out, const void* q_rot, const void* k_
  */
 int kshipra_device_status(int32_t* code_out, void* stream);
 
-/* Process-wide tuning switch (KSHIPRA_OPT_*).  Errors: INVALID_ARG. */
+/* Sets a tuning option (KSHIPRA_OPT_*) for the calling host thread only;
+ * it applies to that thread's later calls.  Errors: INVALID_ARG. */
 int kshipra_set_option(int option, int value);
 
 /* Static description of a status code. */

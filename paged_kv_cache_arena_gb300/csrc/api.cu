@@ -35,8 +35,12 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(KSHIPRA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-std::atomic<int> g_opt_split_tokens{0};
-std::atomic<int> g_opt_decode_max_rows{kDecodeMaxRows};
+// Tuning options (kshipra_set_option), one set per host thread: a thread's
+// calls and its workspace queries see only its own settings, so threads (or
+// libraries) that tune differently never change each other's kernels or
+// workspace sizes.
+thread_local int g_opt_split_tokens = 0;
+thread_local int g_opt_decode_max_rows = kDecodeMaxRows;
 
 // ---- device status word ------------------------------------------------
 __device__ unsigned g_status_word;
@@ -168,7 +172,7 @@ constexpr int kDecodeWaves = 1;
 constexpr int kDecodeMaxSplit = 8192;
 
 int split_tokens_for(int num_seqs, int max_context_len, int num_kv_heads, int sm_count) {
-  const int opt = g_opt_split_tokens.load();
+  const int opt = g_opt_split_tokens;
   if (opt > 0) return opt;
   const long long units = static_cast<long long>(num_seqs) * num_kv_heads;
   const long long target = static_cast<long long>(kDecodeWaves) * 2 * (sm_count > 0 ? sm_count : 1);
@@ -195,7 +199,7 @@ WorkspacePlan plan_workspace(int num_seqs, int num_tokens, int max_context_len, 
   p.split_tokens = split_tokens_for(num_seqs, max_context_len, num_kv_heads, sm_count);
   p.max_splits = max_context_len > 0 ? (max_context_len + p.split_tokens - 1) / p.split_tokens : 1;
   if (p.max_splits < 1) p.max_splits = 1;
-  if (p.max_splits > 1 && g_opt_decode_max_rows.load() > 0) {  // decode partials and counters
+  if (p.max_splits > 1 && g_opt_decode_max_rows > 0) {  // decode partials and counters
     const size_t rows = static_cast<size_t>(p.max_splits) * num_tokens * num_q_heads;
     p.o_bytes = round256(rows * head_dim * sizeof(float));
     p.ml_bytes = round256(rows * 2 * sizeof(float));
@@ -278,7 +282,7 @@ int attention_impl(void* out, const void* q_rot, const void* k_arena, const void
   a.group = num_q_heads / num_kv_heads; a.head_dim = head_dim; a.block_size = block_size;
   a.max_blocks_per_seq = max_blocks_per_seq; a.num_blocks = num_blocks;
   a.split_tokens = plan.split_tokens; a.max_splits = plan.max_splits;
-  a.decode_max_rows = g_opt_decode_max_rows.load();
+  a.decode_max_rows = g_opt_decode_max_rows;
   a.decode_ordered = num_seqs <= kDecodeOrderedMaxSeqs ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.dtype = dtype;
@@ -366,12 +370,12 @@ int kshipra_set_option(int option, int value) {
     case KSHIPRA_OPT_SPLIT_TOKENS:
       if (value < 0 || value % 64)
         return fail(KSHIPRA_ERR_INVALID_ARG, "split tokens %d must be 0 or a positive multiple of 64", value);
-      g_opt_split_tokens.store(value);
+      g_opt_split_tokens = value;
       return KSHIPRA_OK;
     case KSHIPRA_OPT_DECODE_MAX_ROWS:
       if (value < 0 || value > kDecodeMaxRows)
         return fail(KSHIPRA_ERR_INVALID_ARG, "decode max rows %d not in [0, %d]", value, kDecodeMaxRows);
-      g_opt_decode_max_rows.store(value);
+      g_opt_decode_max_rows = value;
       return KSHIPRA_OK;
     default:
       return fail(KSHIPRA_ERR_INVALID_ARG, "unknown option %d", option);
@@ -488,11 +492,11 @@ int kshipra_decode_step(void* out, const void* q, const void* k, const void* v, 
     if (p && !aligned(p, 16)) return fail(KSHIPRA_ERR_INVALID_ARG, "data pointers must be 16-byte aligned");
   if (q_rot && (q_rot == out || q_rot == q)) return fail(KSHIPRA_ERR_INVALID_ARG, "q_rot must not alias out or q");
   const int group = num_q_heads / num_kv_heads;
-  if (static_cast<long long>(max_query_len) * group > g_opt_decode_max_rows.load()) {
+  if (static_cast<long long>(max_query_len) * group > g_opt_decode_max_rows) {
     // rows for the tensor-core prefill kernel: the two steps, through q_rot
     if (!q_rot)
       return fail(KSHIPRA_ERR_INVALID_ARG, "q_rot is required when a sequence has more than %d query rows",
-                  g_opt_decode_max_rows.load());
+                  g_opt_decode_max_rows);
     if ((rc = kshipra_kv_append_rope(q, k, v, q_rot, k_arena, v_arena, block_tables, query_start_loc, positions,
                                      rope_table, rope_max_pos, num_seqs, num_tokens, num_q_heads, num_kv_heads,
                                      head_dim, block_size, max_blocks_per_seq, num_blocks, dtype, stream)))

@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "internal.h"
 
 namespace {
 
@@ -56,7 +57,8 @@ extern "C" int kshipra_paged_attention_noalloc(void* out, const void* q_rot, con
                                                int max_blocks_per_seq, int num_blocks, float scale, int dtype,
                                                void* stream) {
   void* scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) return KSHIPRA_ERR_CUDA;
+  const cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess) return kshipra::api_cuda_fail(e, "looking up the no-alloc scratch address");
   // The workspace check of kshipra_paged_attention rejects sizes whose split
   // partials exceed the scratch (KSHIPRA_ERR_WORKSPACE_TOO_SMALL, message in
   // kshipra_last_error) before anything is launched.  Every partial the
