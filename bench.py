@@ -233,16 +233,6 @@ def time_e2e(torch, dw, steps, stream, fused=False, graph=False):
     return t0.elapsed_time(t1), h2d, d2h
 
 
-# DRAM bytes (read + write) of one decode_kernel launch on the llama-decode
-# workload, from the ncu capture summarised in
-# profiles/decode_kernel_llama-decode.md (the fused step's kernel); reported
-# only for that workload and valid while the kernel is unchanged since its
-# capture (the fused step's kernel, and the attention-only kernel of the
-# two-call step).
-DECODE_TRAFFIC_LLAMA_DECODE = 592119040 + 970752
-DECODE_TRAFFIC_LLAMA_DECODE_TWO_CALL = 591848192 + 249088
-
-
 def gpu_launches_per_step(w, decode_max_rows=16, fused=False):
     """Kernels one step launches, following the library's host-side choices:
     append; decode unless the lengths rule out a decode-class sequence;
@@ -442,6 +432,17 @@ def measure_workload(torch, stream, pk, name, steps=30):
     return out
 
 
+def workload_config(w, world: int) -> dict:
+    """The ``config`` object of the JSON line (the same for both arms)."""
+    kv = decode_kv_bytes(w)
+    return {"workload": w.name, "num_seqs": w.num_seqs,
+            "context_lens": "%d-%d" % (int(w.context_lens.min()), int(w.context_lens.max())),
+            "heads": "%dq/%dkv" % (w.num_q_heads, w.num_kv_heads), "head_dim": w.head_dim,
+            "block_size": w.block_size, "kv_bytes_per_step": kv,
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "inputs larger than L2 (%.0f MB of KV per step)" % (kv / 1e6)}
+
+
 # ------------------------------------------------------------------ oracle (CPU)
 
 def oracle_sample(w, budget_s: float = 15.0):
@@ -496,9 +497,7 @@ def reference_arm(args, w):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "num_seqs": w.num_seqs, "context": "512-4096",
-                       "heads": "%dq/%dkv" % (w.num_q_heads, w.num_kv_heads), "head_dim": w.head_dim,
-                       "block_size": w.block_size, "l2": "n/a (CPU)"},
+            "config": workload_config(w, args.gpus),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": "%d sequences per step, taken in order of the %d-sequence workload "
                                        "(all q heads), float64 C oracle" % (n_seqs, w.num_seqs)},
@@ -615,15 +614,12 @@ def gpu_arm(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16" if w.dtype == "f16" else "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "num_seqs": w.num_seqs, "context_lens": "%d-%d" % (
-                int(w.context_lens.min()), int(w.context_lens.max())),
-                "heads": "%dq/%dkv" % (w.num_q_heads, w.num_kv_heads), "head_dim": w.head_dim,
-                "block_size": w.block_size, "kv_bytes_per_step": kv, "parallelism": "replicas" if world > 1 else "single",
-                "l2": "inputs larger than L2 (%.0f MB of KV per step)" % (kv / 1e6)},
+            "config": workload_config(w, world),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk.get("hbm_gbs"),
                          "unit": "GB/s", "frac": round(achieved / pk.get("hbm_gbs"), 4),
-                         "traffic": (DECODE_TRAFFIC_LLAMA_DECODE if fused else DECODE_TRAFFIC_LLAMA_DECODE_TWO_CALL)
-                         if w.name == "llama-decode" else None,
+                         "traffic": None,
+                         "traffic_note": "DRAM bytes per launch come from an ncu capture of this kernel, not from "
+                                         "this run",
                          "kernel": ("decode step (decode_kernel with RoPE-and-append and split combine inside)"
                                     if fused else "paged attention call (decode_kernel, split combine inside)"),
                          "ms_per_launch": round(att_ms, 5), "peak_source": pk_src},
