@@ -245,7 +245,7 @@ def gpu_launches_per_step(w, decode_max_rows=16, fused=False):
     max_q = int(w.query_lens.max())
     if fused and max_q * G <= decode_max_rows:
         return 1  # kshipra_decode_step: RoPE-and-append inside the decode kernel
-    n = 1  # append
+    n = 1  # append (for a fused step with prefill rows: K and V only)
     qd = decode_max_rows // G
     if qd >= 1 and T <= (S - 1) * max_q + qd:
         n += 1  # decode (splits merged in the same kernel)
@@ -368,9 +368,11 @@ def measure_prefill(torch, stream, pk):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     steps = 50
     total, app, att = time_steps(torch, dw, steps, 5, stream, flush=flush)
-    att_ms = statistics.mean(att)
+    _, _, step = time_steps(torch, dw, steps, 5, stream, flush=flush, fused=True)
+    att_ms, step_ms = statistics.mean(att), statistics.mean(step)
     flops = attention_flops(w)
     tflops = flops / (att_ms * 1e-3) / 1e12
+    step_tflops = flops / (step_ms * 1e-3) / 1e12
     peak = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     return {"workload": "chunked-prefill", "metric": "chunked-prefill attention TFLOP/s", "unit": "TFLOP/s",
             "value": round(tflops, 2), "ms_per_call": round(att_ms, 5), "flops_per_call": flops,
@@ -378,6 +380,11 @@ def measure_prefill(torch, stream, pk):
             "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(tflops / peak, 4), "traffic": None,
                          "peak_note": "fp16 dense = bf16 dense rate (measured cuBLAS bf16 burst)"},
+            "step": {"what": "kshipra_decode_step: K/V append, then the attention kernel rotating q itself "
+                             "(started as the append's programmatic dependent)",
+                     "ms": round(step_ms, 5), "tflops": round(step_tflops, 2), "frac": round(step_tflops / peak, 4),
+                     "two_call_ms": round(statistics.mean(app) + att_ms, 5),
+                     "two_call_frac": round(flops / ((statistics.mean(app) + att_ms) * 1e-3) / 1e12 / peak, 4)},
             "l2": "flushed between calls (512 MiB write)"}
 
 
@@ -401,7 +408,8 @@ def measure_workload(torch, stream, pk, name, steps=30):
     w = make_config(name)
     dw = DeviceWorkload(w)
     _, app, att = time_steps(torch, dw, steps, 5, stream)
-    att_ms, app_ms = statistics.mean(att), statistics.mean(app)
+    _, _, step = time_steps(torch, dw, steps, 5, stream, fused=True)
+    att_ms, app_ms, step_ms = statistics.mean(att), statistics.mean(app), statistics.mean(step)
     dec = decode_class(w)
     pre = np.setdiff1d(np.arange(w.num_seqs), dec)
     kv = decode_kv_bytes(w, dec)
@@ -413,7 +421,10 @@ def measure_workload(torch, stream, pk, name, steps=30):
     ideal_ms = max(kv / (bw * 1e9), flops / (tc * 1e12)) * 1e3
     out = {"workload": name, "num_seqs": w.num_seqs, "query_tokens": int(w.num_tokens),
            "dtype": w.dtype, "block_size": w.block_size, "attention_ms_per_call": round(att_ms, 5),
-           "append_ms_per_call": round(app_ms, 5), "tokens_per_s": round(w.num_tokens / (att_ms * 1e-3), 1),
+           "append_ms_per_call": round(app_ms, 5), "step_ms": round(step_ms, 5),
+           "step": "kshipra_decode_step (one decode launch with the append inside, or a K/V append then "
+                   "attention kernels rotating q themselves)",
+           "tokens_per_s": round(w.num_tokens / (att_ms * 1e-3), 1),
            "decode_seqs": int(len(dec)), "decode_kv_bytes": kv, "prefill_seqs": int(len(pre)),
            "prefill_flops": flops, "l2": "inputs larger than L2 (%.0f MB of KV read per call)" % (kv / 1e6),
            "status": None}

@@ -212,7 +212,8 @@ WorkspacePlan plan_workspace(int num_seqs, int num_tokens, int max_context_len, 
   return p;
 }
 
-// The new tokens' raw rows for the fused decode step (see AttnArgs).
+// The new tokens' raw rows for the fused step (see AttnArgs): k and v NULL
+// when a separate append writes them (the kernels then only rotate q).
 struct FusedInputs {
   const void* q;
   const void* k;
@@ -224,14 +225,17 @@ struct FusedInputs {
   void* v_arena;
 };
 
-// kshipra_paged_attention, or with fz the fused decode step (every sequence
-// of the decode class; q_rot then is an optional output).
+// kshipra_paged_attention, or with fz a fused step (q_rot then is an optional
+// output): every sequence of the decode class with fz->k set (one launch that
+// also appends), or, with fz->k NULL, attention kernels that rotate q after a
+// separate K/V append, launched as its programmatic dependents (dependent).
+// validate_only: return after the host-side checks, before any CUDA work.
 int attention_impl(void* out, const void* q_rot, const void* k_arena, const void* v_arena,
                    const int32_t* block_tables, const int32_t* context_lens, const int32_t* query_start_loc,
                    const int32_t* positions, int num_seqs, int num_tokens, int max_query_len, int max_context_len,
                    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
                    int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream,
-                   const FusedInputs* fz) {
+                   const FusedInputs* fz, bool dependent = false, bool validate_only = false) {
   if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || max_context_len < 0)
     return fail(KSHIPRA_ERR_INVALID_ARG, "negative size argument");
   if (num_seqs == 0 && num_tokens > 0) return fail(KSHIPRA_ERR_INVALID_ARG, "tokens without sequences");
@@ -263,6 +267,9 @@ int attention_impl(void* out, const void* q_rot, const void* k_arena, const void
     return fail(KSHIPRA_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, %zu needed", workspace_bytes, plan.total);
   if (plan.total && (!workspace || !aligned(workspace, 256)))
     return fail(KSHIPRA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
+  if (fz && !fz->k && head_dim != 128)
+    return fail(KSHIPRA_ERR_UNSUPPORTED, "in-kernel query rotation needs head_dim 128");
+  if (validate_only) return KSHIPRA_OK;
 
   AttnArgs a{};
   a.out = out; a.q_rot = q_rot; a.block_tables = block_tables; a.context_lens = context_lens;
@@ -291,6 +298,7 @@ int attention_impl(void* out, const void* q_rot, const void* k_arena, const void
     a.rope_max_pos = fz->rope_max_pos; a.q_rot_out = fz->q_rot_out;
     a.k_arena_w = fz->k_arena; a.v_arena_w = fz->v_arena;
   }
+  a.pdl = dependent ? 1 : 0;
   if ((e = status_ptr(&a.status)) != cudaSuccess) return cuda_fail(e, "status word");
 
   const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
@@ -315,7 +323,7 @@ int attention_impl(void* out, const void* q_rot, const void* k_arena, const void
     CUtensorMap kmap_p, vmap_p;
     if ((rc = arena_map(&kmap_p, k_arena, dtype, head_dim, rows, block_size))) return rc;
     if ((rc = arena_map(&vmap_p, v_arena, dtype, head_dim, rows, block_size))) return rc;
-    if ((rc = query_map(&qmap, q_rot, dtype, head_dim, num_q_heads, num_tokens, a.group))) return rc;
+    if ((rc = query_map(&qmap, fz ? fz->q : q_rot, dtype, head_dim, num_q_heads, num_tokens, a.group))) return rc;
     if ((e = launch_prefill(a, kmap_p, vmap_p, qmap, s)) != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
   }
   return KSHIPRA_OK;
@@ -439,6 +447,7 @@ int kshipra_kv_append_rope(const void* q, const void* k, const void* v, void* q_
   a.num_blocks = num_blocks; a.dtype = dtype;
   cudaError_t e = status_ptr(&a.status);
   if (e != cudaSuccess) return cuda_fail(e, "status word");
+  if ((e = sm_count_current(&a.sm_count)) != cudaSuccess) return cuda_fail(e, "SM count");
   e = launch_append_rope(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
   return KSHIPRA_OK;
@@ -492,8 +501,28 @@ int kshipra_decode_step(void* out, const void* q, const void* k, const void* v, 
     if (p && !aligned(p, 16)) return fail(KSHIPRA_ERR_INVALID_ARG, "data pointers must be 16-byte aligned");
   if (q_rot && (q_rot == out || q_rot == q)) return fail(KSHIPRA_ERR_INVALID_ARG, "q_rot must not alias out or q");
   const int group = num_q_heads / num_kv_heads;
+  if (static_cast<long long>(max_query_len) * group > g_opt_decode_max_rows && head_dim == 128) {
+    // rows for the tensor-core prefill kernel: the K/V append, then attention
+    // kernels that rotate q themselves (q_rot optional) and start while the
+    // append finishes; every host check runs before the append is enqueued
+    const FusedInputs fz{q, nullptr, nullptr, rope_table, rope_max_pos, q_rot, k_arena, v_arena};
+    if ((rc = attention_impl(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc, positions,
+                             num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads, num_kv_heads,
+                             head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype, workspace,
+                             workspace_bytes, stream, &fz, true, true)))
+      return rc;
+    if ((rc = kshipra_kv_append_rope(nullptr, k, v, nullptr, k_arena, v_arena, block_tables, query_start_loc,
+                                     positions, rope_table, rope_max_pos, num_seqs, num_tokens, num_q_heads,
+                                     num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, dtype,
+                                     stream)))
+      return rc;
+    return attention_impl(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc, positions,
+                          num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads, num_kv_heads, head_dim,
+                          block_size, max_blocks_per_seq, num_blocks, scale, dtype, workspace, workspace_bytes, stream,
+                          &fz, true, false);
+  }
   if (static_cast<long long>(max_query_len) * group > g_opt_decode_max_rows) {
-    // rows for the tensor-core prefill kernel: the two steps, through q_rot
+    // head_dim 64 with prefill rows: the two calls, through q_rot
     if (!q_rot)
       return fail(KSHIPRA_ERR_INVALID_ARG, "q_rot is required when a sequence has more than %d query rows",
                   g_opt_decode_max_rows);

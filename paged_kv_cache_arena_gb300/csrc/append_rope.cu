@@ -36,6 +36,10 @@ constexpr int kUnitsInFlight = 2;  // units a thread loads before any is stored
 // instead of following one another.
 template <bool kBf16>
 __global__ void __launch_bounds__(kAppendThreads, 16) append_rope_kernel(AppendArgs a) {
+  // an attention grid launched after this one as its programmatic dependent
+  // may start its own preparation now; it waits for this grid's completion
+  // before reading the arena
+  grid_launch_dependents();
   const int t = blockIdx.x;
   if (t >= a.num_tokens) return;
   const int pos = __ldg(a.positions + t);

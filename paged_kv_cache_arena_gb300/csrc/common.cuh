@@ -11,6 +11,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 #include "../../include/kshipra.h"
 
@@ -522,7 +523,45 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
       : "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+//
+// A grid launched with programmatic stream serialization may start while the
+// grid before it on the stream is still running.  It must wait here before it
+// reads anything that grid writes; a grid launched the ordinary way returns
+// at once.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allows the grid launched after this one (with programmatic stream
+// serialization) to start once every CTA of this grid has run this or
+// exited; it still waits for this grid's completion before reading its
+// writes.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- host
+
+// Launches kernel<<<grid, block, smem, stream>>>(args...); with `dependent`
+// set, as a programmatic dependent of the previous grid on the stream (the
+// kernel then calls grid_dependency_wait() before reading what that grid
+// writes, and every CTA calls it before exiting so that the grid's
+// completion implies the previous one's).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 bool dependent, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (dependent) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 
 // Raises a kernel's dynamic shared-memory limit once per device.
 template <typename Kernel>

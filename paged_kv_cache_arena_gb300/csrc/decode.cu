@@ -33,7 +33,8 @@
 //    workspace, and the CTA that finishes last for its (sequence, kv head)
 //    (atomic ticket) merges all splits.
 //  - Fused decode step (kshipra_decode_step): the kernel also does the
-//    RoPE-and-append of the step's new tokens.  Each CTA rotates its own query
+//    RoPE-and-append of the step's new tokens (or, in a mixed step whose
+//    append ran as its own kernel, only the query rotation).  Each CTA rotates its own query
 //    rows from the raw q in registers; in the CTA whose split holds a new
 //    token's position, the warp that loads the chunk holding it writes that
 //    token's rotated K and raw V (its kv head) into the arena before it loads
@@ -103,7 +104,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap* kmap, const CUten
     // tile; the other warps start at once
     constexpr int half = D / 2;
     bool wrote = false;
-    for (int i = 0; i < qlen; ++i) {
+    for (int i = 0; a.k_new != nullptr && i < qlen; ++i) {
       const int t = q0 + i;
       const int pos = __ldg(a.positions + t);
       if (pos < tok_begin || pos >= tok_end || ((pos - tok_begin) / kChunk) % kWarps != warp) continue;
@@ -569,6 +570,9 @@ template <int D, bool kBf16, bool kFused>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const AttnArgs a) {
+  // launched after the step's append as its programmatic dependent, every CTA
+  // waits for it (so this grid completes after it) before reading the arena
+  grid_dependency_wait();
   int s, h, split;
   if (!decode_unit(a, s, h, split)) return;
   const int q0 = __ldg(a.query_start_loc + s);
@@ -593,8 +597,8 @@ cudaError_t launch_decode_f(const AttnArgs& a, const CUtensorMap& kmap, const CU
   // at most max_splits units per (sequence, kv head); CTAs past the last unit exit at once
   const long long units = static_cast<long long>(a.max_splits) * a.num_kv_heads * a.num_seqs;
   if (units > INT_MAX) return cudaErrorInvalidConfiguration;
-  decode_kernel<D, kBf16, kFused><<<static_cast<unsigned>(units), kThreads, L::kAlloc, stream>>>(kmap, vmap, a);
-  return cudaGetLastError();
+  return launch_kernel(decode_kernel<D, kBf16, kFused>, dim3(static_cast<unsigned>(units)), dim3(kThreads), L::kAlloc,
+                       stream, a.pdl != 0, kmap, vmap, a);
 }
 
 template <int D, bool kBf16>

@@ -34,6 +34,7 @@ struct AppendArgs {
   int rope_max_pos;
   int num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks;
   int dtype;
+  int sm_count;  // of the device the call runs on (sizes the grid)
   unsigned* status;
 };
 
@@ -62,10 +63,11 @@ struct AttnArgs {
   int decode_ordered;            // decode CTAs take their units longest first (num_seqs <= kDecodeOrderedMaxSeqs)
   float scale_log2;              // scale * log2(e)
   int dtype;
-  // fused decode step: when q_raw is set the decode kernel rotates the query
-  // rows itself (q_raw [T][Hq][d]) and writes the new tokens' rotated K and raw
-  // V (k_new, v_new [T][Hkv][d]) into the arena before reading it; q_rot_out
-  // (optional) receives the rotated q.
+  // fused step: when q_raw is set the attention kernels rotate the query rows
+  // themselves (q_raw [T][Hq][d]; q_rot is then unused) and q_rot_out
+  // (optional) receives the rotated q.  The decode kernel also writes the new
+  // tokens' rotated K and raw V (k_new, v_new [T][Hkv][d]) into the arena
+  // before reading it, unless k_new is NULL (a separate append wrote them).
   const void* q_raw;
   const void* k_new;
   const void* v_new;
@@ -74,6 +76,9 @@ struct AttnArgs {
   void* q_rot_out;
   void* k_arena_w;
   void* v_arena_w;
+  // launch the attention kernels as programmatic dependents of the previous
+  // grid on the stream (they wait for it before reading the arena)
+  int pdl;
 };
 
 // Batches of at most this many sequences run their decode units longest

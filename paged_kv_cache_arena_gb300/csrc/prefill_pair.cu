@@ -39,12 +39,20 @@
 //    memory in the MMA's operand layout; each warp reports "S read", "P
 //    ready" and "O read" to the leader with one remote arrival.
 // TMEM (each CTA): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// Fused step (q_raw set): Q_A / Q_B are loaded from the raw (unrotated) q
+// and land on a barrier of their own CTA; each softmax thread rotates its row
+// in shared memory (the append kernel's float32 arithmetic, bit for bit),
+// optionally stores it to q_rot, and the MMA issuers start on "Q ready"
+// instead of "Q landed".  Launched as a programmatic dependent of the step's
+// K/V append, the kernel plans its work and loads and rotates Q while the
+// append finishes, and waits for it only before the first K/V load.
 // Every wait is bounded; on a timeout all roles stop and drain their own
 // outstanding copies / MMAs before the pair releases tensor memory.
 #include <float.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "rope.cuh"
 
 namespace kshipra {
 namespace {
@@ -73,7 +81,7 @@ struct Layout {
   static constexpr int kK = kPB + kPTile;
   static constexpr int kV = kK + kStages * kKStage;
   static constexpr int kBar = kV + kStages * kVStage;
-  static constexpr int kNumBars = 2 + 4 * kStages + 14 + 2;
+  static constexpr int kNumBars = 2 + 4 * kStages + 14 + 2 + 3;
   static constexpr int kPlan = kBar + kNumBars * 8 + 16;  // work list planned in the kernel
   static constexpr int kPlanSorted = kPlan;                 // [kSortCapacity] sorted entries
   static constexpr int kPlanBuf = kPlanSorted + kSortCapacity * 8;  // [kSortCapacity] listed entries
@@ -102,6 +110,8 @@ struct Bars {
   uint64_t* o_full;    // [2] both: O_x complete for the item
   uint64_t* o_free;    // [2] leader, 8 warp arrivals: O_x read by the epilogue
   uint64_t* drain;     // [2] leader: per issuer
+  uint64_t* q_land;    // own CTA (fused step): this CTA's raw Q_A, Q_B landed
+  uint64_t* q_ready;   // [2] leader (fused step), 8 warp arrivals: Q_x rotated in both CTAs
 };
 
 __device__ __forceinline__ Bars bars_at(uint8_t* smem) {
@@ -120,6 +130,8 @@ __device__ __forceinline__ Bars bars_at(uint8_t* smem) {
   b.o_full = b.p_free + 4;
   b.o_free = b.o_full + 2;
   b.drain = b.o_free + 2;
+  b.q_land = b.drain + 2;
+  b.q_ready = b.q_land + 1;
   return b;
 }
 
@@ -267,6 +279,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_pair_plan_kernel(const A
   __shared__ int base;
   const int total = plan_entries<G, kPlanThreads>(a, buf, warp_total, &base, entries, max_entries);
   if (threadIdx.x == 0) *count = total * a.num_kv_heads;
+  grid_dependency_wait();  // this grid completes after the one it depends on
 }
 
 // ---------------------------------------------------------------- producer
@@ -302,7 +315,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
   const int my_blk = k_lane ? k_first + kblk : (v_lane ? vblk : -1);
   int g = 0;  // key tiles issued by this CTA
   int items_done = 0;
-  bool ok = true;
+  bool ok = true, waited = false;
+  const bool rotate = a.q_raw != nullptr;
   for (int r = 0; ok; ++r) {
     const int idx = item_index(r);
     if (idx >= count) break;
@@ -315,14 +329,26 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
     const int32_t* table = a.block_tables + static_cast<size_t>(it.s) * a.max_blocks_per_seq;
     int next_id = lane_block_id(table, 0, p.nkeys, bs, my_blk);
     if (items_done > 0 && !warp_wait(b.q_empty, (items_done - 1) & 1, a.status)) { ok = false; break; }
-    if (leader && lane == 0) mbar_arrive_expect_tx(b.q_full, 4 * L::kQTile);  // both CTAs, zero-filled rows included
+    if (rotate) {  // raw Q onto this CTA's own barrier: the softmax warps rotate it in place
+      if (lane == 0) mbar_arrive_expect_tx(b.q_land, 2 * L::kQTile);
+    } else if (leader && lane == 0) {
+      mbar_arrive_expect_tx(b.q_full, 4 * L::kQTile);  // both CTAs, zero-filled rows included
+    }
     __syncwarp();
     if (lane < 4) {
       const int reg = lane & 1, tb = lane >> 1;
-      tma_load_3d_pair(smem + (tb ? L::kQB : L::kQA) + reg * L::kQRegion, qmap, 64 * reg, it.h * G,
-                       p.q0 + p.tok + TQ * tb, map_to_rank(b.q_full, 0));
+      uint8_t* qdst = smem + (tb ? L::kQB : L::kQA) + reg * L::kQRegion;
+      if (rotate)
+        tma_load_3d(qdst, qmap, 64 * reg, it.h * G, p.q0 + p.tok + TQ * tb, b.q_land);
+      else
+        tma_load_3d_pair(qdst, qmap, 64 * reg, it.h * G, p.q0 + p.tok + TQ * tb, map_to_rank(b.q_full, 0));
     }
     ++items_done;
+    if (!waited) {  // the arena may still be written by the grid this one depends on
+      grid_dependency_wait();
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      waited = true;
+    }
     for (int j = 0; j < p.ntiles; ++j, ++g) {
       const int st = g % kStages, use = g / kStages;
       const int id = next_id;
@@ -464,7 +490,10 @@ __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const
     const QuadGeom p = quad_geom<G>(a, it.s, it.quad, 0);
     const int n = p.ntiles;
     if (n == 0) continue;
-    if (!mbar_wait_cluster(b.q_full, items_done & 1, a.status)) { ok = false; break; }
+    if (!mbar_wait_cluster(a.q_raw != nullptr ? &b.q_ready[x] : b.q_full, items_done & 1, a.status)) {
+      ok = false;
+      break;
+    }
     const int g0 = g;
     // the item's first scores, once the previous tile's S columns are read
     if (!mbar_wait_cluster(&b.kv_full[g0 % kStages], (g0 / kStages) & 1, a.status) ||
@@ -619,6 +648,39 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
     const int tok = row_valid ? p.q0 + p.tok + TQ * x + tl : p.q0 + p.last;
     const int pos = __ldg(a.positions + tok);
     float m_ref = kNegInf, l = 0.f;
+    if (a.q_raw != nullptr) {
+      // fused step: rotate this row of the raw Q_x in place (both 64-column
+      // regions: element e in region 0 pairs with e + 64 in region 1, at the
+      // same swizzled chunk), store it to q_rot when asked, and report Q_x
+      // ready to the issuer
+      if (!warp_wait(b.q_land, items_done & 1, a.status)) { ok = false; break; }
+      if (row_valid) {
+        if (pos < 0 || pos >= a.rope_max_pos) {
+          report(a.status, KSHIPRA_DEV_BAD_POSITION);
+        } else {
+          uint8_t* qrow = smem + (x ? L::kQB : L::kQA) + r * 128;
+          const float* cs = a.rope_table + static_cast<size_t>(pos) * kD;
+          uint16_t* qr_out = a.q_rot_out == nullptr ? nullptr
+                                                    : static_cast<uint16_t*>(a.q_rot_out) +
+                                                          (static_cast<size_t>(tok) * a.num_q_heads + it.h * G + gg) * kD;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4* lo = reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4));
+            uint4* hi = reinterpret_cast<uint4*>(qrow + L::kQRegion + ((c ^ (r & 7)) << 4));
+            uint4 ylo, yhi;
+            rotate_eight_pairs_vals<kBf16>(*lo, *hi, cs + 16 * c, ylo, yhi);
+            *lo = ylo;
+            *hi = yhi;
+            if (qr_out != nullptr) {
+              reinterpret_cast<uint4*>(qr_out)[c] = ylo;
+              reinterpret_cast<uint4*>(qr_out + kD / 2)[c] = yhi;
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();  // the rotated rows visible to the tensor cores
+      warp_arrive_leader(map_to_rank(&b.q_ready[x], 0));
+    }
 
     for (int j = 0; j < n; ++j) {
       const int gt = g + j;
@@ -743,7 +805,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     count = *planned_count;
   }
-  if (static_cast<int>(blockIdx.x >> 1) >= count) return;  // no item for this pair (same test in both CTAs)
+  if (static_cast<int>(blockIdx.x >> 1) >= count) {  // no item for this pair (same test in both CTAs)
+    grid_dependency_wait();  // this grid completes after the one it depends on
+    return;
+  }
   const Bars b = bars_at(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + L::kNumBars * 8);
   const uint32_t rank = cluster_rank();
@@ -769,6 +834,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(&b.drain[0], 1);
     mbar_init(&b.drain[1], 1);
+    mbar_init(b.q_land, 1);
+    mbar_init(&b.q_ready[0], 2 * 4);
+    mbar_init(&b.q_ready[1], 2 * 4);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -788,6 +856,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (rank == 0) {
     if (lane == 0) mma_role<kBf16, G>(a, smem, b, tmem, items, count, warp - kMmaWarp);
   }
+  grid_dependency_wait();  // (at once when the producer has waited already)
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // no CTA leaves while its peer may still signal its barriers
@@ -828,13 +897,17 @@ cudaError_t launch_pair_t(const AttnArgs& a, const CUtensorMap& kmap, const CUte
   if (e != cudaSuccess) return e;
   const int clusters = pair_clusters(prefill_pair_kernel<kBf16, G>, a.sm_count);
   const bool plan_here = a.max_items <= kSortCapacity;  // an upper bound on the entries
+  // as a programmatic dependent (fused step), the first grid of the two waits
+  // for the append; the attention kernel that reads the planned list then
+  // follows the planning kernel the ordinary way
   if (!plan_here) {
-    prefill_pair_plan_kernel<G><<<1, kPlanThreads, 0, stream>>>(a, a.ws_items, a.ws_item_count, a.max_items);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_kernel(prefill_pair_plan_kernel<G>, dim3(1), dim3(kPlanThreads), 0, stream, a.pdl != 0, a, a.ws_items,
+                      a.ws_item_count, a.max_items);
+    if (e != cudaSuccess) return e;
   }
-  prefill_pair_kernel<kBf16, G><<<2 * clusters, kThreads, Layout::kAlloc, stream>>>(
-      kmap, vmap, qmap, a, a.ws_items, a.ws_item_count, plan_here ? 1 : 0);
-  return cudaGetLastError();
+  return launch_kernel(prefill_pair_kernel<kBf16, G>, dim3(2 * clusters), dim3(kThreads), Layout::kAlloc, stream,
+                       a.pdl != 0 && plan_here, kmap, vmap, qmap, a, static_cast<const uint64_t*>(a.ws_items),
+                       static_cast<const int*>(a.ws_item_count), plan_here ? 1 : 0);
 }
 
 template <bool kBf16>

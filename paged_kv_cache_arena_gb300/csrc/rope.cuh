@@ -1,4 +1,5 @@
-// RoPE rotation shared by the append kernel and the fused decode step.
+// RoPE rotation shared by the append kernel, the fused decode step and the
+// prefill kernel's in-place query rotation.
 //
 // Pages "Building Kshipra" part 3 (kshipra-3), section 4: new tokens are
 // rotated at their absolute positions.  Pairs (i, i + d/2) rotate by the
@@ -52,17 +53,15 @@ __device__ __forceinline__ void rotate_two_pairs(const uint16_t* src, uint16_t* 
   *reinterpret_cast<uint32_t*>(dst + i + half) = rope_pair<kBf16>(hi, lo, t, true);
 }
 
-// Rotates pairs (e + k, e + k + d/2), k = 0..7, of one head row into dst
-// with 16-byte stores (e a multiple of 8, e < d/2; rows 16-byte aligned),
-// from the row's words already loaded (lo: elements e.., hi: e + d/2..); cs
-// is the position's [d/2][2] table row.  Each element is rotated exactly as
-// rope_pair rotates it.
+// Rotated pairs (e + k, e + k + d/2), k = 0..7, of one head row: lo holds
+// elements e.., hi elements e + d/2..; cs_e points at the (cos, sin) entries
+// of frequencies e.. (the position's table row + 2 e).  Each element is
+// rotated exactly as rope_pair rotates it.
 template <bool kBf16>
-__device__ __forceinline__ void rotate_eight_pairs(uint4 lo, uint4 hi, uint16_t* dst, int e, int half,
-                                                   const float* cs) {
-  const float4* c4 = reinterpret_cast<const float4*>(cs + 2 * e);
+__device__ __forceinline__ void rotate_eight_pairs_vals(uint4 lo, uint4 hi, const float* cs_e, uint4& ylo,
+                                                        uint4& yhi) {
+  const float4* c4 = reinterpret_cast<const float4*>(cs_e);
   const float4 t0 = __ldg(c4), t1 = __ldg(c4 + 1), t2 = __ldg(c4 + 2), t3 = __ldg(c4 + 3);
-  uint4 ylo, yhi;
   ylo.x = rope_pair<kBf16>(lo.x, hi.x, t0, false);
   ylo.y = rope_pair<kBf16>(lo.y, hi.y, t1, false);
   ylo.z = rope_pair<kBf16>(lo.z, hi.z, t2, false);
@@ -71,6 +70,17 @@ __device__ __forceinline__ void rotate_eight_pairs(uint4 lo, uint4 hi, uint16_t*
   yhi.y = rope_pair<kBf16>(hi.y, lo.y, t1, true);
   yhi.z = rope_pair<kBf16>(hi.z, lo.z, t2, true);
   yhi.w = rope_pair<kBf16>(hi.w, lo.w, t3, true);
+}
+
+// Rotates pairs (e + k, e + k + d/2), k = 0..7, of one head row into dst
+// with 16-byte stores (e a multiple of 8, e < d/2; rows 16-byte aligned),
+// from the row's words already loaded (lo: elements e.., hi: e + d/2..); cs
+// is the position's [d/2][2] table row.
+template <bool kBf16>
+__device__ __forceinline__ void rotate_eight_pairs(uint4 lo, uint4 hi, uint16_t* dst, int e, int half,
+                                                   const float* cs) {
+  uint4 ylo, yhi;
+  rotate_eight_pairs_vals<kBf16>(lo, hi, cs + 2 * e, ylo, yhi);
   *reinterpret_cast<uint4*>(dst + e) = ylo;
   *reinterpret_cast<uint4*>(dst + e + half) = yhi;
 }

@@ -23,6 +23,19 @@ CASES = {
 }
 
 
+def _many_sequences():
+    # more sequences than an append CTA has threads, with runs of empty ones:
+    # a run of tokens whose sequences lie more than 256 entries apart
+    # (sequence 0 ends at token 350, sequences 1-300 have no new token,
+    # sequence 301 starts at token 351), and 400 more short sequences
+    qlen = [351] + [0] * 300 + [349] + [1, 0] * 200
+    prefix = [3] + [5] * 300 + [20] + [7, 2] * 200
+    return custom(7, Hq=8, Hkv=2, prefix=prefix, qlen=qlen, spare=4)
+
+
+CASES["many-sequences"] = _many_sequences
+
+
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_arena_and_q_rot_bit_exact(clean_status, name):
     w = CASES[name]()

@@ -115,4 +115,4 @@ def test_full_and_last_splits_in_one_batch(clean_status, split, copies):
     ctx = [64, 128, 192, 65, 129, 1, 100, 100, 63, 256] * copies
     w = custom(37, Hq=8, Hkv=2, prefix=[c - 1 for c in ctx], qlen=[1] * len(ctx))
     dw = run(w, split=split)
-    assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype, "full and last splits")
+    assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype, "split order (%d sequences)" % len(ctx))

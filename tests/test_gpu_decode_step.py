@@ -1,8 +1,10 @@
-"""kshipra_decode_step (RoPE-and-append fused into the decode kernel) on the
-GPU: the same arena image and rotated q, bit for bit, as the append kernel
-and the oracle (pages "Building Kshipra" part 3: section 1 block arena,
-section 4 RoPE at absolute positions), and attention within tolerance of the
-float64 oracle and bit-identical to the two-call path."""
+"""kshipra_decode_step on the GPU: for decode batches RoPE-and-append fused
+into the decode kernel, for batches with prefill rows a K/V append followed by
+attention kernels that rotate q themselves.  The same arena image and rotated
+q, bit for bit, as the append kernel and the oracle (pages "Building Kshipra"
+part 3: section 1 block arena, section 4 RoPE at absolute positions), and
+attention within tolerance of the float64 oracle and bit-identical to the
+two-call path."""
 
 import numpy as np
 import pytest
@@ -84,9 +86,63 @@ def test_without_q_rot_buffer(clean_status):
     assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype, "no q_rot")
 
 
-def test_prefill_rows_take_the_two_calls(clean_status):
-    # a chunk of 40 tokens is beyond the decode kernel: append + attention
-    w = custom(48, Hq=8, Hkv=2, prefix=[10, 300], qlen=[40, 1])
+PREFILL_CASES = {
+    # batches with prefill-class rows: a K/V-only append, then attention
+    # kernels that rotate q themselves (head_dim 128), decode rows included
+    "chunked-prefill": lambda: make_config("chunked-prefill"),
+    "mixed": lambda: make_config("mixed"),
+    "g1": lambda: custom(61, Hq=4, Hkv=4, prefix=[5, 250], qlen=[130, 40]),
+    "g2": lambda: custom(62, Hq=8, Hkv=4, prefix=[300, 0, 77], qlen=[260, 513, 31]),
+    "g8-bs32-bf16": lambda: custom(63, Hq=16, Hkv=2, bs=32, dtype="bf16", prefix=[33, 400], qlen=[20, 3]),
+    "g16-bs32": lambda: custom(64, Hq=32, Hkv=2, bs=32, prefix=[64, 7], qlen=[9, 30]),
+    "shared-prefix": lambda: custom(65, Hq=8, Hkv=2, prefix=[64, 96, 200], qlen=[40, 1, 70], shared_len=64,
+                                    shared=(0, 1, 2)),
+    # more work-list entries than the attention kernel plans itself: the
+    # planning kernel runs first
+    "1030-chunks": lambda: custom(36, Hq=8, Hkv=2, prefix=[(7 * k) % 23 for k in range(1030)], qlen=[5] * 1030),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_CASES))
+def test_fused_prefill_step(clean_status, name):
+    w = PREFILL_CASES[name]()
+    dw = fused(w)
+    ka, va = oracle.workload_arena(w, NAN_SENTINEL)
+    assert np.array_equal(bits_of(dw.k_arena), ka)
+    assert np.array_equal(bits_of(dw.v_arena), va)
+    assert np.array_equal(bits_of(dw.q_rot), oracle.workload_q_rot(w))
+    what = ("full %s (fused step)" % name) if name in ("chunked-prefill", "mixed") else name
+    assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype, what)
+    ref = two_calls(w)
+    assert np.array_equal(bits_of(dw.out), bits_of(ref.out))
+
+
+def test_fused_prefill_step_without_q_rot(clean_status):
+    w = custom(66, prefix=[10, 300, 0], qlen=[140, 1, 64])
+    dw = fused(w, q_rot=False)
+    ka, va = oracle.workload_arena(w, NAN_SENTINEL)
+    assert np.array_equal(bits_of(dw.k_arena), ka) and np.array_equal(bits_of(dw.v_arena), va)
+    assert np.array_equal(bits_of(dw.out), bits_of(two_calls(w).out))
+
+
+def test_fused_prefill_steps_in_a_row(clean_status):
+    # consecutive steps on one stream: each step's attention starts while its
+    # own append finishes, never before the previous step is done
+    w = custom(67, prefix=[0, 700], qlen=[300, 129])
+    dw = DeviceWorkload(w)
+    outs = []
+    for _ in range(4):
+        dw.decode_step()
+        outs.append(dw.out.clone())
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert np.array_equal(bits_of(o), bits_of(outs[0]))
+    assert_close(outs[0].float().cpu().numpy().astype(np.float64), oracle.workload_attention(w), w.dtype, "in a row")
+
+
+def test_prefill_rows_head_dim_64_take_the_two_calls(clean_status):
+    # head_dim 64 (one-CTA prefill kernel): append + attention through q_rot
+    w = custom(48, Hq=8, Hkv=2, d=64, prefix=[10, 300], qlen=[40, 1])
     dw = fused(w)
     ka, va = oracle.workload_arena(w, NAN_SENTINEL)
     assert np.array_equal(bits_of(dw.k_arena), ka)
