@@ -126,6 +126,24 @@ def _events(torch, n):
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
 
+def time_loop(torch, fn, steps, warmup, stream):
+    """Milliseconds of `steps` back-to-back calls of fn on `stream`, bracketed
+    by one pair of CUDA events (no event between the calls, so consecutive
+    kernels may overlap their launch as they would in a serving loop)."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+    torch.cuda.synchronize()
+    t0, t1 = _events(torch, 2)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(steps):
+            fn()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1)
+
+
 def time_steps(torch, dw, steps, warmup, stream, flush=None, fused=False):
     """Times `steps` whole steps on `stream`: append + attention as two calls,
     or (fused) one kshipra_decode_step call.
@@ -396,8 +414,9 @@ def decode_class(w, decode_max_rows=16):
 
 
 def measure_workload(torch, stream, pk, name, steps=30):
-    """Secondary object for one more config: its attention call timed on the
-    launching stream (the append of its new tokens timed beside it), inputs
+    """Secondary object for one more config: its attention calls timed back
+    to back on the launching stream (the append of its new tokens timed
+    beside it, and the whole step through kshipra_decode_step), inputs
     larger than L2.  Decode-class sequences are measured in KV GB/s against
     HBM, prefill-class ones in TFLOP/s against the dense tensor peak; a
     mixed batch runs both kernels in one call, and its fraction is the
@@ -407,9 +426,11 @@ def measure_workload(torch, stream, pk, name, steps=30):
     from workloads.device import DeviceWorkload
     w = make_config(name)
     dw = DeviceWorkload(w)
-    _, app, att = time_steps(torch, dw, steps, 5, stream)
-    _, _, step = time_steps(torch, dw, steps, 5, stream, fused=True)
-    att_ms, app_ms, step_ms = statistics.mean(att), statistics.mean(app), statistics.mean(step)
+    _, app, _ = time_steps(torch, dw, steps, 5, stream)
+    # attention calls back to back (inputs larger than L2), one pair of events
+    att_ms = time_loop(torch, lambda: dw.attention(stream=stream), steps, 5, stream) / steps
+    step_ms = time_loop(torch, lambda: dw.decode_step(stream=stream), steps, 5, stream) / steps
+    app_ms = statistics.mean(app)
     dec = decode_class(w)
     pre = np.setdiff1d(np.arange(w.num_seqs), dec)
     kv = decode_kv_bytes(w, dec)
@@ -564,17 +585,24 @@ def gpu_arm(args, w):
         smi_id = str(local)
     barrier()
     torch.cuda.synchronize()
+    step_fn = (lambda: dw.decode_step(stream=stream)) if fused else (lambda: dw.step(stream=stream))
     with ClockSampler(smi_id) as clk:
         barrier()
-        total_ms, app, att = time_steps(torch, dw, args.steps, args.warmup, stream, fused=fused)
+        total_ms = time_loop(torch, step_fn, args.steps, args.warmup, stream)
         barrier()
     clocks = clk.summary()
+    own_ms = total_ms
     if world > 1:
         total_ms = max_over_ranks(torch, dist, total_ms, "cuda")
     status = K.kshipra_device_status()
     ms_step = total_ms / args.steps
     value = job_throughput(world, kv, args.steps, total_ms)
-    att_ms = statistics.mean(att)
+    # per-call breakdown (an event around each call), a shorter pass of its own
+    _, app, att = time_steps(torch, dw, min(args.steps, 200), 3, stream, fused=fused)
+    # the fused step is one launch per step: its average launch duration is
+    # the timed loop's time per step; the two-call step's attention call is
+    # timed by its own events
+    att_ms = own_ms / args.steps if fused else statistics.mean(att)
     achieved = kv / (att_ms * 1e-3) / 1e9
     e2e_steps = min(args.steps, 300)
     e2e_ms, h2d, d2h = time_e2e(torch, dw, e2e_steps, stream, fused=fused)

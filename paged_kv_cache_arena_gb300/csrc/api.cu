@@ -298,7 +298,7 @@ int attention_impl(void* out, const void* q_rot, const void* k_arena, const void
     a.rope_max_pos = fz->rope_max_pos; a.q_rot_out = fz->q_rot_out;
     a.k_arena_w = fz->k_arena; a.v_arena_w = fz->v_arena;
   }
-  a.pdl = dependent ? 1 : 0;
+  a.early_inputs = dependent ? 1 : 0;
   if ((e = status_ptr(&a.status)) != cudaSuccess) return cuda_fail(e, "status word");
 
   const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;

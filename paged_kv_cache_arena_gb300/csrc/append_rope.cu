@@ -36,10 +36,11 @@ constexpr int kUnitsInFlight = 2;  // units a thread loads before any is stored
 // instead of following one another.
 template <bool kBf16>
 __global__ void __launch_bounds__(kAppendThreads, 16) append_rope_kernel(AppendArgs a) {
-  // an attention grid launched after this one as its programmatic dependent
-  // may start its own preparation now; it waits for this grid's completion
-  // before reading the arena
+  // launched as a programmatic dependent of the previous grid on the stream:
+  // the next grid (the step's attention) may start its own preparation now,
+  // and this one waits for the previous grid before touching memory
   grid_launch_dependents();
+  grid_dependency_wait();
   const int t = blockIdx.x;
   if (t >= a.num_tokens) return;
   const int pos = __ldg(a.positions + t);
@@ -162,11 +163,8 @@ cudaError_t launch_append_rope(const AppendArgs& a, cudaStream_t stream) {
   // CTAs; a long one (a prefill chunk) keeps one CTA per token
   const int per_token = a.num_tokens >= 512 ? 1 : (units + kAppendThreads - 1) / kAppendThreads;
   dim3 grid(a.num_tokens, per_token), block(kAppendThreads);
-  if (a.dtype == KSHIPRA_DTYPE_BF16)
-    append_rope_kernel<true><<<grid, block, 0, stream>>>(a);
-  else
-    append_rope_kernel<false><<<grid, block, 0, stream>>>(a);
-  return cudaGetLastError();
+  return a.dtype == KSHIPRA_DTYPE_BF16 ? launch_kernel(append_rope_kernel<true>, grid, block, 0, stream, true, a)
+                                       : launch_kernel(append_rope_kernel<false>, grid, block, 0, stream, true, a);
 }
 
 }  // namespace kshipra

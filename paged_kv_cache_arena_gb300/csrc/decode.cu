@@ -570,8 +570,10 @@ template <int D, bool kBf16, bool kFused>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const AttnArgs a) {
-  // launched after the step's append as its programmatic dependent, every CTA
-  // waits for it (so this grid completes after it) before reading the arena
+  // launched as a programmatic dependent of the previous grid on the stream:
+  // the next grid may start its own launch now, and every CTA waits for the
+  // previous one (so this grid completes after it) before touching memory
+  grid_launch_dependents();
   grid_dependency_wait();
   int s, h, split;
   if (!decode_unit(a, s, h, split)) return;
@@ -598,7 +600,7 @@ cudaError_t launch_decode_f(const AttnArgs& a, const CUtensorMap& kmap, const CU
   const long long units = static_cast<long long>(a.max_splits) * a.num_kv_heads * a.num_seqs;
   if (units > INT_MAX) return cudaErrorInvalidConfiguration;
   return launch_kernel(decode_kernel<D, kBf16, kFused>, dim3(static_cast<unsigned>(units)), dim3(kThreads), L::kAlloc,
-                       stream, a.pdl != 0, kmap, vmap, a);
+                       stream, true, kmap, vmap, a);
 }
 
 template <int D, bool kBf16>

@@ -76,9 +76,12 @@ struct AttnArgs {
   void* q_rot_out;
   void* k_arena_w;
   void* v_arena_w;
-  // launch the attention kernels as programmatic dependents of the previous
-  // grid on the stream (they wait for it before reading the arena)
-  int pdl;
+  // every kernel of the library launches as a programmatic dependent of the
+  // previous grid on the stream and waits for it before touching memory it
+  // may write; with early_inputs set (the fused step, whose predecessor is
+  // the library's own K/V append) the attention kernels read everything but
+  // the arena before that wait
+  int early_inputs;
 };
 
 // Batches of at most this many sequences run their decode units longest

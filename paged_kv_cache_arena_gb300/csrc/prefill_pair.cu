@@ -277,6 +277,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_pair_plan_kernel(const A
   __shared__ uint64_t buf[kSortCapacity];
   __shared__ int warp_total[kPlanThreads / 32];
   __shared__ int base;
+  grid_launch_dependents();
+  if (!a.early_inputs) grid_dependency_wait();  // the lengths may come from the previous grid
   const int total = plan_entries<G, kPlanThreads>(a, buf, warp_total, &base, entries, max_entries);
   if (threadIdx.x == 0) *count = total * a.num_kv_heads;
   grid_dependency_wait();  // this grid completes after the one it depends on
@@ -795,6 +797,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // (saves a launch), else by the planning kernel
   const uint64_t* items = planned;
   int count;
+  grid_launch_dependents();
+  // launched as a programmatic dependent of the previous grid on the stream:
+  // wait for it before touching memory, unless this is the fused step
+  // (predecessor: the library's K/V append) and the work list is planned
+  // here, when only the arena must wait (the producer waits before its first
+  // K/V load)
+  if (!a.early_inputs || !plan_here) grid_dependency_wait();
   if (plan_here) {
     uint64_t* sorted = reinterpret_cast<uint64_t*>(smem + L::kPlanSorted);
     int* warp_total = reinterpret_cast<int*>(smem + L::kPlanWarp);
@@ -897,16 +906,15 @@ cudaError_t launch_pair_t(const AttnArgs& a, const CUtensorMap& kmap, const CUte
   if (e != cudaSuccess) return e;
   const int clusters = pair_clusters(prefill_pair_kernel<kBf16, G>, a.sm_count);
   const bool plan_here = a.max_items <= kSortCapacity;  // an upper bound on the entries
-  // as a programmatic dependent (fused step), the first grid of the two waits
-  // for the append; the attention kernel that reads the planned list then
-  // follows the planning kernel the ordinary way
+  // both launch as programmatic dependents; the attention kernel waits for
+  // the planning kernel before reading the planned list
   if (!plan_here) {
-    e = launch_kernel(prefill_pair_plan_kernel<G>, dim3(1), dim3(kPlanThreads), 0, stream, a.pdl != 0, a, a.ws_items,
+    e = launch_kernel(prefill_pair_plan_kernel<G>, dim3(1), dim3(kPlanThreads), 0, stream, true, a, a.ws_items,
                       a.ws_item_count, a.max_items);
     if (e != cudaSuccess) return e;
   }
   return launch_kernel(prefill_pair_kernel<kBf16, G>, dim3(2 * clusters), dim3(kThreads), Layout::kAlloc, stream,
-                       a.pdl != 0 && plan_here, kmap, vmap, qmap, a, static_cast<const uint64_t*>(a.ws_items),
+                       true, kmap, vmap, qmap, a, static_cast<const uint64_t*>(a.ws_items),
                        static_cast<const int*>(a.ws_item_count), plan_here ? 1 : 0);
 }
 
