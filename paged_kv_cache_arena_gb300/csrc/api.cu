@@ -212,6 +212,39 @@ WorkspacePlan plan_workspace(int num_seqs, int num_tokens, int max_context_len, 
   return p;
 }
 
+// Host checks of kshipra_kv_append_rope and its launch arguments.
+int append_prepare(AppendArgs* out, const void* q, const void* k, const void* v, void* q_rot, void* k_arena,
+                   void* v_arena, const int32_t* block_tables, const int32_t* query_start_loc,
+                   const int32_t* positions, const float* rope_table, int rope_max_pos, int num_seqs, int num_tokens,
+                   int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                   int num_blocks, int dtype) {
+  if (num_seqs < 0 || num_tokens < 0) return fail(KSHIPRA_ERR_INVALID_ARG, "negative num_seqs or num_tokens");
+  if (num_seqs == 0 && num_tokens > 0) return fail(KSHIPRA_ERR_INVALID_ARG, "tokens without sequences");
+  int rc = check_heads(num_q_heads, num_kv_heads, head_dim, block_size, dtype);
+  if (rc) return rc;
+  if ((rc = check_arena(num_blocks, num_kv_heads, block_size, max_blocks_per_seq))) return rc;
+  if ((q == nullptr) != (q_rot == nullptr))
+    return fail(KSHIPRA_ERR_INVALID_ARG, "q and q_rot must both be given or both be NULL");
+  if (rope_max_pos <= 0) return fail(KSHIPRA_ERR_INVALID_ARG, "rope_max_pos must be positive");
+  if (num_tokens == 0) return KSHIPRA_OK;
+  if (!k || !v || !k_arena || !v_arena || !block_tables || !query_start_loc || !positions || !rope_table)
+    return fail(KSHIPRA_ERR_INVALID_ARG, "a required pointer is NULL");
+  const void* vec[] = {q, k, v, q_rot, k_arena, v_arena, rope_table};
+  for (const void* p : vec)
+    if (p && !aligned(p, 16)) return fail(KSHIPRA_ERR_INVALID_ARG, "data pointers must be 16-byte aligned");
+  AppendArgs& a = *out;
+  a.q = q; a.k = k; a.v = v; a.q_rot = q_rot; a.k_arena = k_arena; a.v_arena = v_arena;
+  a.block_tables = block_tables; a.query_start_loc = query_start_loc; a.positions = positions;
+  a.rope_table = rope_table; a.rope_max_pos = rope_max_pos;
+  a.num_seqs = num_seqs; a.num_tokens = num_tokens; a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim; a.block_size = block_size; a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks; a.dtype = dtype;
+  cudaError_t e = status_ptr(&a.status);
+  if (e != cudaSuccess) return cuda_fail(e, "status word");
+  if ((e = sm_count_current(&a.sm_count)) != cudaSuccess) return cuda_fail(e, "SM count");
+  return KSHIPRA_OK;
+}
+
 // The new tokens' raw rows for the fused step (see AttnArgs): k and v NULL
 // when a separate append writes them (the kernels then only rotate q).
 struct FusedInputs {
@@ -424,31 +457,12 @@ int kshipra_kv_append_rope(const void* q, const void* k, const void* v, void* q_
                            int num_tokens, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                            int max_blocks_per_seq, int num_blocks, int dtype, void* stream) {
   g_last_error[0] = 0;
-  if (num_seqs < 0 || num_tokens < 0) return fail(KSHIPRA_ERR_INVALID_ARG, "negative num_seqs or num_tokens");
-  if (num_seqs == 0 && num_tokens > 0) return fail(KSHIPRA_ERR_INVALID_ARG, "tokens without sequences");
-  int rc = check_heads(num_q_heads, num_kv_heads, head_dim, block_size, dtype);
-  if (rc) return rc;
-  if ((rc = check_arena(num_blocks, num_kv_heads, block_size, max_blocks_per_seq))) return rc;
-  if ((q == nullptr) != (q_rot == nullptr))
-    return fail(KSHIPRA_ERR_INVALID_ARG, "q and q_rot must both be given or both be NULL");
-  if (rope_max_pos <= 0) return fail(KSHIPRA_ERR_INVALID_ARG, "rope_max_pos must be positive");
-  if (num_tokens == 0) return KSHIPRA_OK;
-  if (!k || !v || !k_arena || !v_arena || !block_tables || !query_start_loc || !positions || !rope_table)
-    return fail(KSHIPRA_ERR_INVALID_ARG, "a required pointer is NULL");
-  const void* vec[] = {q, k, v, q_rot, k_arena, v_arena, rope_table};
-  for (const void* p : vec)
-    if (p && !aligned(p, 16)) return fail(KSHIPRA_ERR_INVALID_ARG, "data pointers must be 16-byte aligned");
   AppendArgs a{};
-  a.q = q; a.k = k; a.v = v; a.q_rot = q_rot; a.k_arena = k_arena; a.v_arena = v_arena;
-  a.block_tables = block_tables; a.query_start_loc = query_start_loc; a.positions = positions;
-  a.rope_table = rope_table; a.rope_max_pos = rope_max_pos;
-  a.num_seqs = num_seqs; a.num_tokens = num_tokens; a.num_q_heads = num_q_heads; a.num_kv_heads = num_kv_heads;
-  a.head_dim = head_dim; a.block_size = block_size; a.max_blocks_per_seq = max_blocks_per_seq;
-  a.num_blocks = num_blocks; a.dtype = dtype;
-  cudaError_t e = status_ptr(&a.status);
-  if (e != cudaSuccess) return cuda_fail(e, "status word");
-  if ((e = sm_count_current(&a.sm_count)) != cudaSuccess) return cuda_fail(e, "SM count");
-  e = launch_append_rope(a, static_cast<cudaStream_t>(stream));
+  int rc = append_prepare(&a, q, k, v, q_rot, k_arena, v_arena, block_tables, query_start_loc, positions, rope_table,
+                          rope_max_pos, num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
+                          max_blocks_per_seq, num_blocks, dtype);
+  if (rc || num_tokens == 0) return rc;
+  const cudaError_t e = launch_append_rope(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
   return KSHIPRA_OK;
 }
@@ -511,11 +525,15 @@ int kshipra_decode_step(void* out, const void* q, const void* k, const void* v, 
                              head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype, workspace,
                              workspace_bytes, stream, &fz, true, true)))
       return rc;
-    if ((rc = kshipra_kv_append_rope(nullptr, k, v, nullptr, k_arena, v_arena, block_tables, query_start_loc,
-                                     positions, rope_table, rope_max_pos, num_seqs, num_tokens, num_q_heads,
-                                     num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, dtype,
-                                     stream)))
+    AppendArgs ap{};
+    if ((rc = append_prepare(&ap, nullptr, k, v, nullptr, k_arena, v_arena, block_tables, query_start_loc, positions,
+                             rope_table, rope_max_pos, num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim,
+                             block_size, max_blocks_per_seq, num_blocks, dtype)))
       return rc;
+    if (num_tokens > 0) {
+      const cudaError_t e = launch_append_rope(ap, static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
+    }
     return attention_impl(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc, positions,
                           num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads, num_kv_heads, head_dim,
                           block_size, max_blocks_per_seq, num_blocks, scale, dtype, workspace, workspace_bytes, stream,

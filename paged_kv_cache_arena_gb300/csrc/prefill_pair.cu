@@ -44,8 +44,9 @@
 // in shared memory (the append kernel's float32 arithmetic, bit for bit),
 // optionally stores it to q_rot, and the MMA issuers start on "Q ready"
 // instead of "Q landed".  Launched as a programmatic dependent of the step's
-// K/V append, the kernel plans its work and loads and rotates Q while the
-// append finishes, and waits for it only before the first K/V load.
+// K/V append, the kernel plans its work, loads and rotates Q and reads the
+// cached-prefix key tiles while the append finishes, and waits for it only
+// before the first key tile that reaches the sequence's new positions.
 // Every wait is bounded; on a timeout all roles stop and drain their own
 // outstanding copies / MMAs before the pair releases tensor memory.
 #include <float.h>
@@ -317,7 +318,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
   const int my_blk = k_lane ? k_first + kblk : (v_lane ? vblk : -1);
   int g = 0;  // key tiles issued by this CTA
   int items_done = 0;
-  bool ok = true, waited = false;
+  // outside the fused step the kernel waited for its predecessor at the start
+  bool ok = true, waited = !a.early_inputs;
   const bool rotate = a.q_raw != nullptr;
   for (int r = 0; ok; ++r) {
     const int idx = item_index(r);
@@ -346,11 +348,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
         tma_load_3d_pair(qdst, qmap, 64 * reg, it.h * G, p.q0 + p.tok + TQ * tb, map_to_rank(b.q_full, 0));
     }
     ++items_done;
-    if (!waited) {  // the arena may still be written by the grid this one depends on
-      grid_dependency_wait();
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      waited = true;
-    }
+    // fused step: the K/V append this grid depends on writes the sequence's
+    // positions from p_new on (its query tokens); key tiles below p_new hold
+    // earlier appends only and are read while the append still runs
+    const int p_new = waited ? 0 : __ldg(a.positions + p.q0);
     for (int j = 0; j < p.ntiles; ++j, ++g) {
       const int st = g % kStages, use = g / kStages;
       const int id = next_id;
@@ -370,6 +371,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
           row = (id * a.num_kv_heads + it.h) * bs;
       }
       if (g >= kStages && !warp_wait(&b.kv_empty[st], (use - 1) & 1, a.status)) { ok = false; break; }
+      if (!waited && kTile * (j + 1) > p_new) {  // the tile reaches the new positions
+        grid_dependency_wait();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        waited = true;
+      }
       if (lane == 0) {
         // the leader expects both CTAs' K halves and, but for the last tile,
         // both V halves; an item's last V tile lands on each CTA's v_last,
