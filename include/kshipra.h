@@ -303,22 +303,30 @@ int kshipra_paged_attention(void* out, const void* q_rot, const void* k_arena, c
                             void* stream);
 
 /*
- * One decode step: kshipra_kv_append_rope followed by
- * kshipra_paged_attention (kshipra-3, sections 1 and 4), with the same
- * arguments and results -- the arena gets the new tokens' rotated K and raw V
- * bit for bit as the append writes them, out is the attention of the
- * rotated q -- in ONE launch when every sequence is of the decode class
- * (max_query_len x group <= KSHIPRA_OPT_DECODE_MAX_ROWS): each decode CTA
- * rotates its query rows from q in registers, and in the CTA whose key split
- * holds a new token's position the warp that reads that position writes the
- * token's K and V first.  Otherwise the two calls run one after the other.
+ * One step: kshipra_kv_append_rope followed by kshipra_paged_attention
+ * (kshipra-3, sections 1 and 4), with the same arguments and results -- the
+ * arena gets the new tokens' rotated K and raw V bit for bit as the append
+ * writes them, out is the attention of the rotated q, bit for bit as the two
+ * calls give it -- with fewer launches and no q_rot round trip:
+ *  - every sequence of the decode class (max_query_len x group <=
+ *    KSHIPRA_OPT_DECODE_MAX_ROWS): ONE launch; each decode CTA rotates its
+ *    query rows from q in registers, and in the CTA whose key split holds a
+ *    new token's position the warp that reads that position writes the
+ *    token's K and V first;
+ *  - otherwise, head_dim 128: the append writes K and V only, then the
+ *    attention kernels rotate q themselves (the prefill kernel in shared
+ *    memory, the decode kernel in registers) and start while the append
+ *    finishes.  This relies on no sequence's new tokens landing in a block
+ *    that another sequence of the call reads as its cached prefix (a shared
+ *    block is copied before it is written: kshipra_block_make_private);
+ *  - otherwise (head_dim 64): the two calls, one after the other.
  *
  * q [num_tokens][num_q_heads][head_dim], k, v [num_tokens][num_kv_heads]
  * [head_dim], rope_table as for kshipra_kv_append_rope; the other arguments
  * as for kshipra_paged_attention, with the same workspace size.  q_rot
  * (device, [num_tokens][num_q_heads][head_dim]) receives the rotated q; it
- * may be NULL on the one-launch path and is required otherwise.  q_rot must
- * not alias out or q.
+ * may be NULL except for head_dim 64 batches with prefill-class rows.  q_rot
+ * must not alias out or q.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA.
  */
 int kshipra_decode_step(void* out, const void* q, const void* k, const void* v, void* q_rot, void* k_arena,
