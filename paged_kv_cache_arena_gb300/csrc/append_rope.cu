@@ -37,10 +37,12 @@ constexpr int kUnitsInFlight = 2;  // units a thread loads before any is stored
 template <bool kBf16>
 __global__ void __launch_bounds__(kAppendThreads, 16) append_rope_kernel(AppendArgs a) {
   // launched as a programmatic dependent of the previous grid on the stream:
-  // the next grid (the step's attention) may start its own preparation now,
-  // and this one waits for the previous grid before touching memory
-  grid_launch_dependents();
+  // wait for it before touching memory, then let the next grid (the step's
+  // attention) start its own preparation.  In that order, the next grid
+  // launches only once the previous one has completed, so it may read
+  // anything but what this grid writes (the arena) before it waits
   grid_dependency_wait();
+  grid_launch_dependents();
   const int t = blockIdx.x;
   if (t >= a.num_tokens) return;
   const int pos = __ldg(a.positions + t);

@@ -79,8 +79,9 @@ struct AttnArgs {
   // every kernel of the library launches as a programmatic dependent of the
   // previous grid on the stream and waits for it before touching memory it
   // may write; with early_inputs set (the fused step, whose predecessor is
-  // the library's own K/V append) the attention kernels read everything but
-  // the arena before that wait
+  // the library's own K/V append, which lets its dependents launch only after
+  // its own predecessor has completed) the attention kernels read everything
+  // but the arena before that wait
   int early_inputs;
 };
 

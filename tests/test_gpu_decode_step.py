@@ -13,7 +13,7 @@ import torch
 import oracle
 from helpers import assert_close, custom, random_decode
 from workloads import make_config
-from workloads.device import NAN_SENTINEL, DeviceWorkload, bits_of
+from workloads.device import NAN_SENTINEL, DeviceWorkload, bits_of, to_device_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -138,6 +138,30 @@ def test_fused_prefill_steps_in_a_row(clean_status):
     for o in outs[1:]:
         assert np.array_equal(bits_of(o), bits_of(outs[0]))
     assert_close(outs[0].float().cpu().numpy().astype(np.float64), oracle.workload_attention(w), w.dtype, "in a row")
+
+
+def test_fused_prefill_step_sees_inputs_written_just_before(clean_status):
+    # the step's attention kernels read q, positions and tables before they
+    # wait for the K/V append: those inputs must still be the ones that the
+    # kernels queued before the step wrote -- here q is overwritten by a copy
+    # on the same stream right before each step
+    w = custom(68, prefix=[0, 900, 2000], qlen=[256, 384, 128])
+    w2 = custom(69, prefix=[0, 900, 2000], qlen=[256, 384, 128])
+    dw = DeviceWorkload(w)
+    q_a = dw.q.clone()
+    q_b = to_device_bits(w2.q, dw.q.dtype, "cuda")
+    for _ in range(3):
+        dw.q.copy_(q_b)
+        dw.decode_step()
+        out_b = dw.out.clone()
+        dw.q.copy_(q_a)
+        dw.decode_step()
+        out_a = dw.out.clone()
+    torch.cuda.synchronize()
+    ref = two_calls(w)
+    assert np.array_equal(bits_of(out_a), bits_of(ref.out))
+    w.q = w2.q
+    assert_close(out_b.float().cpu().numpy().astype(np.float64), oracle.workload_attention(w), w.dtype, "q from b")
 
 
 def test_prefill_rows_head_dim_64_take_the_two_calls(clean_status):
