@@ -1,0 +1,64 @@
+"""Calls that follow each other on one stream, each reading what the one
+before wrote (the way one layer's attention output feeds the next layer):
+every kernel of the library starts as a programmatic dependent of the grid
+before it and must still see that grid's writes.  Each chain runs once with
+nothing between the calls and once with a device synchronisation between
+them; the outputs must be bit-identical."""
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import custom, random_decode
+from workloads.device import DeviceWorkload, bits_of
+
+pytestmark = pytest.mark.gpu
+
+
+def _attention(K, dw, out, q_rot):
+    w = dw.w
+    K.kshipra_paged_attention(out, q_rot, dw.k_arena, dw.v_arena, dw.block_tables, dw.context_lens,
+                              dw.query_start_loc, dw.positions, w.max_query_len, w.max_context_len, w.scale,
+                              dw.workspace)
+
+
+def _step(K, dw, out, q):
+    w = dw.w
+    K.kshipra_decode_step(out, q, dw.k_new, dw.v_new, None, dw.k_arena, dw.v_arena, dw.block_tables,
+                          dw.context_lens, dw.query_start_loc, dw.positions, dw.rope_table, w.max_query_len,
+                          w.max_context_len, w.scale, dw.workspace)
+
+
+def _chain(K, dw, call, sync, links=4):
+    outs = [torch.empty_like(dw.q) for _ in range(links)]
+    src = dw.q_rot
+    for o in outs:
+        call(K, dw, o, src)
+        if sync:
+            torch.cuda.synchronize()
+        src = o
+    torch.cuda.synchronize()
+    return [bits_of(o) for o in outs]
+
+
+CASES = {
+    "decode": lambda: random_decode(71, 12, 300, 3000),
+    "prefill": lambda: custom(72, prefix=[100, 300, 0], qlen=[130, 70, 256]),
+    "mixed": lambda: custom(73, prefix=[100, 600, 2000, 40], qlen=[200, 1, 1, 64]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("call", ["attention", "step"])
+def test_each_call_sees_the_previous_output(clean_status, name, call):
+    K = clean_status
+    fn = _attention if call == "attention" else _step
+    dw = DeviceWorkload(CASES[name]())
+    dw.append_step()
+    torch.cuda.synchronize()
+    free = _chain(K, dw, fn, sync=False)
+    synced = _chain(K, dw, fn, sync=True)
+    for a, b in zip(free, synced):
+        assert np.array_equal(a, b)
+    # the chain is not trivial: each link changes the values
+    assert not np.array_equal(free[0], free[1])
