@@ -298,6 +298,37 @@ def test_bruteforce_matches_oracle(oracle_mod, make):
     assert np.max(np.abs(got - np.array(ref))) < 1e-12
 
 
+def _random_micro(seed):
+    """A random micro batch: group size, head_dim, block size, dtype, prefix
+    and chunk lengths, shared prefix blocks and spare blocks drawn from a
+    seeded generator."""
+    rng = np.random.default_rng(500 + seed)
+    Hkv = int(rng.integers(1, 3))
+    G = int(rng.choice([1, 2, 4]))
+    d = int(rng.choice([4, 8, 16]))
+    bs = int(rng.choice([2, 4, 8]))
+    S = int(rng.integers(1, 4))
+    prefix = [int(rng.integers(0, 14)) for _ in range(S)]
+    qlen = [int(rng.integers(1, 6)) for _ in range(S)]
+    shared_len, shared = 0, ()
+    members = [i for i in range(S) if prefix[i] >= bs]
+    if len(members) >= 2 and rng.random() < 0.5:
+        shared_len, shared = bs, tuple(members)
+    theta = float(rng.choice([1.0e4, 5.0e5]))
+    return small(600 + seed, G * Hkv, Hkv, d, bs, str(rng.choice(["f16", "bf16"])), prefix, qlen,
+                 spare=int(rng.integers(0, 4)), shared_len=shared_len, shared=shared, theta=theta)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_bruteforce_matches_oracle_random(oracle_mod, seed):
+    w = _random_micro(seed)
+    got = oracle_mod.workload_attention(w)
+    ref = brute.attention(w.q.tolist(), w.k_all.tolist(), w.v_all.tolist(), w.prefix_lens.tolist(),
+                          w.query_lens.tolist(), w.block_tables.tolist(), w.block_size, w.num_kv_heads, w.theta,
+                          w.scale, w.dtype)
+    assert np.max(np.abs(got - np.array(ref))) < 1e-12
+
+
 def _rotated_f64(oracle_mod, w):
     """q and k rotated in float64 through the oracle's table (test restatement)."""
     tab = oracle_mod.rope_table(w.max_context_len + 1, w.head_dim, w.theta)
