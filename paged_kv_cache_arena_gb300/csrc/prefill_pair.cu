@@ -37,7 +37,10 @@
 //  - warps 0-3 / 4-7: softmax of tile A / B of their own CTA, one thread per
 //    row: the whole S row is read into registers once; P goes to shared
 //    memory in the MMA's operand layout; each warp reports "S read", "P
-//    ready" and "O read" to the leader with one remote arrival.
+//    ready" and "O read" to the leader with one remote arrival.  The
+//    epilogue stages O / l in the tile's P buffer and each warp then writes
+//    whole output rows (two per store instruction), as does the fused step's
+//    q_rot store from Q_x.
 // TMEM (each CTA): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Fused step (q_raw set): Q_A / Q_B are loaded from the raw (unrotated) q
 // and land on a barrier of their own CTA; each softmax thread rotates its row
@@ -618,6 +621,33 @@ __device__ __forceinline__ void exp_store(const uint32_t (&t)[32], uint64_t c2x2
   }
 }
 
+// Rows 32 w .. 32 w + 31 of a 128-row tile held in shared memory in the Q
+// layout (columns 0-63 in region 0, 64-127 in region 1, 128-byte swizzle) to
+// their global rows: row t G + gg goes to dst0 + t tok_stride + gg D.  Each
+// half-warp writes one whole 256-byte row per pass (lane L: 16-byte chunk
+// L % 16 of row 32 w + 2 k + L / 16), so that a store instruction covers two
+// rows instead of 32 scattered pieces; rows of tokens t >= nvalid are
+// skipped.  Called by warp w after its lanes wrote their rows (and a warp
+// synchronisation).
+template <int G>
+__device__ __forceinline__ void store_rows(const uint8_t* tile, int w, uint16_t* dst0, size_t tok_stride,
+                                           int nvalid) {
+  const int lane = threadIdx.x & 31, c = lane & 15;
+  const uint8_t* src = tile + (c >> 3) * Layout::kQRegion;
+  uint4 v[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int row = 32 * w + 2 * k + (lane >> 4);
+    v[k] = *reinterpret_cast<const uint4*>(src + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int row = 32 * w + 2 * k + (lane >> 4);
+    if (row / G < nvalid)
+      *reinterpret_cast<uint4*>(dst0 + (row / G) * tok_stride + (row % G) * kD + 8 * c) = v[k];
+  }
+}
+
 // Thread r of tile x owns row r (TMEM lane r): it reads its whole S row once
 // (releasing the S columns to the next QK MMAs at once), masks, finds the row
 // maximum, and writes P to row r of its P tile in shared memory.  The
@@ -638,39 +668,59 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
   const uint32_t o_tmem = tmem + 2 * kTile + kTile * x + lane_off;
   const uint32_t p_row = smem_u32(smem + (x ? L::kPB : L::kPA)) + r * 128;
   const float c2 = a.scale_log2;
-  const int tl = r / G, gg = r % G;
+  const int tl = r / G;
+  const size_t tok_stride = static_cast<size_t>(a.num_q_heads) * kD;
+  uint8_t* const q_tile = smem + (x ? L::kQB : L::kQA);
+  uint8_t* const p_tile = smem + (x ? L::kPB : L::kPA);
   int g = 0, items_done = 0;
   bool ok = true;
 
-  for (int ri = 0; ok; ++ri) {
-    const int idx = item_index(ri);
-    if (idx >= count) break;
-    const Item it = item_at(items, idx, a.num_kv_heads);
-    const QuadGeom p = quad_geom<G>(a, it.s, it.quad, static_cast<int>(rank));
-    const int n = p.ntiles;
-    if (n == 0) continue;
-    const int nvalid = x == 0 ? p.n_a : p.n_b;
+  // The first non-empty item from round ri on, with this row's token and
+  // position (-1 when there is none).  The next item's is read while the last
+  // PV MMAs of the current one run, ahead of its epilogue.
+  struct RowItem {
+    Item it;
+    QuadGeom p;
+    int nvalid, pos;
+  };
+  auto find = [&](int ri, RowItem& w) -> int {
+    for (;; ++ri) {
+      const int idx = item_index(ri);
+      if (idx >= count) return -1;
+      w.it = item_at(items, idx, a.num_kv_heads);
+      w.p = quad_geom<G>(a, w.it.s, w.it.quad, static_cast<int>(rank));
+      if (w.p.ntiles == 0) continue;
+      w.nvalid = x == 0 ? w.p.n_a : w.p.n_b;
+      // rows past the last token compute on whatever the tile holds, at the
+      // position of the quad's last token, and are never stored
+      const int tok = tl < w.nvalid ? w.p.q0 + w.p.tok + TQ * x + tl : w.p.q0 + w.p.last;
+      w.pos = __ldg(a.positions + tok);
+      return ri;
+    }
+  };
+
+  RowItem cur;
+  int ri = find(0, cur);
+  while (ri >= 0) {
+    const Item it = cur.it;
+    const QuadGeom p = cur.p;
+    const int n = p.ntiles, nvalid = cur.nvalid, pos = cur.pos;
     const bool row_valid = tl < nvalid;
-    // rows past the last token compute on whatever the tile holds, at the
-    // position of the quad's last token, and are never stored
-    const int tok = row_valid ? p.q0 + p.tok + TQ * x + tl : p.q0 + p.last;
-    const int pos = __ldg(a.positions + tok);
+    // this tile's first row in the [token][head][D] outputs
+    const size_t row0 = (static_cast<size_t>(p.q0 + p.tok + TQ * x) * a.num_q_heads + it.h * G) * kD;
     float m_ref = kNegInf, l = 0.f;
     if (a.q_raw != nullptr) {
       // fused step: rotate this row of the raw Q_x in place (both 64-column
       // regions: element e in region 0 pairs with e + 64 in region 1, at the
-      // same swizzled chunk), store it to q_rot when asked, and report Q_x
-      // ready to the issuer
+      // same swizzled chunk), store the tile to q_rot when asked, and report
+      // Q_x ready to the issuer
       if (!warp_wait(b.q_land, items_done & 1, a.status)) { ok = false; break; }
       if (row_valid) {
         if (pos < 0 || pos >= a.rope_max_pos) {
           report(a.status, KSHIPRA_DEV_BAD_POSITION);
         } else {
-          uint8_t* qrow = smem + (x ? L::kQB : L::kQA) + r * 128;
+          uint8_t* qrow = q_tile + r * 128;
           const float* cs = a.rope_table + static_cast<size_t>(pos) * kD;
-          uint16_t* qr_out = a.q_rot_out == nullptr ? nullptr
-                                                    : static_cast<uint16_t*>(a.q_rot_out) +
-                                                          (static_cast<size_t>(tok) * a.num_q_heads + it.h * G + gg) * kD;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint4* lo = reinterpret_cast<uint4*>(qrow + ((c ^ (r & 7)) << 4));
@@ -679,12 +729,12 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
             rotate_eight_pairs_vals<kBf16>(*lo, *hi, cs + 16 * c, ylo, yhi);
             *lo = ylo;
             *hi = yhi;
-            if (qr_out != nullptr) {
-              reinterpret_cast<uint4*>(qr_out)[c] = ylo;
-              reinterpret_cast<uint4*>(qr_out + kD / 2)[c] = yhi;
-            }
           }
         }
+      }
+      if (a.q_rot_out != nullptr) {
+        __syncwarp();
+        store_rows<G>(q_tile, quarter, static_cast<uint16_t*>(a.q_rot_out) + row0, tok_stride, nvalid);
       }
       fence_proxy_async_smem();  // the rotated rows visible to the tensor cores
       warp_arrive_leader(map_to_rank(&b.q_ready[x], 0));
@@ -761,11 +811,13 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
     }
     if (!ok) break;
     g += n;
+    RowItem nxt;
+    const int ri_next = find(ri + 1, nxt);
+    // epilogue: O_x / l through P_x (free once O_x is final: every PV MMA of
+    // the item is done), then whole rows to the output
     if (!warp_wait(&b.o_full[x], items_done & 1, a.status)) { ok = false; break; }
     tc_fence_after();
     const float inv = 1.f / l;
-    uint16_t* dst =
-        static_cast<uint16_t*>(a.out) + (static_cast<size_t>(tok) * a.num_q_heads + it.h * G + gg) * kD;
 #pragma unroll
     for (int c = 0; c < kD / 32; ++c) {
       uint32_t t[32];
@@ -774,14 +826,21 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         w[i] = pack2<kBf16>(__uint_as_float(t[2 * i]) * inv, __uint_as_float(t[2 * i + 1]) * inv);
-      if (row_valid) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      for (int i = 0; i < 4; ++i) {
+        const int ch = 4 * c + i;  // 16-byte chunk of the row
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(p_row + (ch >> 3) * L::kQRegion +
+                                                                    (((ch & 7) ^ (r & 7)) << 4)),
+                     "r"(w[4 * i]), "r"(w[4 * i + 1]), "r"(w[4 * i + 2]), "r"(w[4 * i + 3])
+                     : "memory");
       }
     }
-    warp_arrive_leader(map_to_rank(&b.o_free[x], 0));
+    warp_arrive_leader(map_to_rank(&b.o_free[x], 0));  // O_x is read (the warp is synchronised)
+    store_rows<G>(p_tile, quarter, static_cast<uint16_t*>(a.out) + row0, tok_stride, nvalid);
+    __syncwarp();  // every lane's reads of P_x done before the next item writes it
     ++items_done;
+    cur = nxt;
+    ri = ri_next;
   }
 }
 
