@@ -229,8 +229,11 @@ __device__ int plan_entries(const AttnArgs& a, uint64_t* buf, int* warp_total, i
     if (s < a.num_seqs) {
       q0 = __ldg(a.query_start_loc + s);
       qlen = __ldg(a.query_start_loc + s + 1) - q0;
-      if (q0 >= 0 && qlen > 0 && q0 + qlen <= a.num_tokens && qlen * G > a.decode_max_rows)
+      if (q0 >= 0 && qlen > 0 && q0 + qlen <= a.num_tokens && qlen * G > a.decode_max_rows) {
         quads = ceil_div(qlen, 4 * TQ);
+        // read again by every CTA's roles for their items' geometry
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.context_lens + s));
+      }
     }
     int incl = quads;  // inclusive scan within the warp
 #pragma unroll
@@ -245,6 +248,7 @@ __device__ int plan_entries(const AttnArgs& a, uint64_t* buf, int* warp_total, i
     int o = before + incl - quads;
     for (int q = 0; q < quads; ++q, ++o) {
       const int last = min(qlen, 4 * TQ * (q + 1)) - 1;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a.positions + q0 + 4 * TQ * q));
       const int nkeys = __ldg(a.positions + q0 + last) + 1;
       const uint32_t cost = static_cast<uint32_t>(min(max(ceil_div(nkeys, kTile), 0), 0xFFFF));
       if (o >= max_entries) continue;
@@ -855,39 +859,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled layouts need 1024-byte alignment
+    grid_dependency_wait();
     if (threadIdx.x == 0) report(a.status, KSHIPRA_DEV_TIMEOUT);
-    return;
-  }
-  // the work list: planned here, in shared memory, when it is short enough
-  // (saves a launch), else by the planning kernel
-  const uint64_t* items = planned;
-  int count;
-  grid_launch_dependents();
-  // launched as a programmatic dependent of the previous grid on the stream:
-  // wait for it before touching memory, unless this is the fused step
-  // (predecessor: the library's K/V append) and the work list is planned
-  // here, when only the arena must wait (the producer waits before its first
-  // K/V load)
-  if (!a.early_inputs || !plan_here) grid_dependency_wait();
-  if (plan_here) {
-    uint64_t* sorted = reinterpret_cast<uint64_t*>(smem + L::kPlanSorted);
-    int* warp_total = reinterpret_cast<int*>(smem + L::kPlanWarp);
-    const int total = plan_entries<G, kThreads>(a, reinterpret_cast<uint64_t*>(smem + L::kPlanBuf), warp_total,
-                                                warp_total + 12, sorted, kSortCapacity);
-    count = total * a.num_kv_heads;
-    items = sorted;
-  } else {
-    count = *planned_count;
-  }
-  if (static_cast<int>(blockIdx.x >> 1) >= count) {  // no item for this pair (same test in both CTAs)
-    grid_dependency_wait();  // this grid completes after the one it depends on
     return;
   }
   const Bars b = bars_at(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + L::kNumBars * 8);
   const uint32_t rank = cluster_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
+  grid_launch_dependents();
+  // barriers, tensor memory and the cluster handshake touch no global memory:
+  // they run before the wait for the previous grid (launched as its
+  // programmatic dependent, this CTA may start while that grid finishes)
   if (threadIdx.x == 0) {
     mbar_init(b.q_full, 1);
     mbar_init(b.q_empty, 2);
@@ -922,6 +905,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // both CTAs' barriers exist before any remote arrival or copy
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // the work list: planned here, in shared memory, when it is short enough
+  // (saves a launch), else by the planning kernel.  Wait for the previous
+  // grid before touching memory, unless this is the fused step (predecessor:
+  // the library's K/V append) and the work list is planned here, when only
+  // the arena must wait (the producer waits before its first K/V load).
+  // A pair without an item runs its roles zero times.
+  const uint64_t* items = planned;
+  int count;
+  if (!a.early_inputs || !plan_here) grid_dependency_wait();
+  if (plan_here) {
+    uint64_t* sorted = reinterpret_cast<uint64_t*>(smem + L::kPlanSorted);
+    int* warp_total = reinterpret_cast<int*>(smem + L::kPlanWarp);
+    const int total = plan_entries<G, kThreads>(a, reinterpret_cast<uint64_t*>(smem + L::kPlanBuf), warp_total,
+                                                warp_total + 12, sorted, kSortCapacity);
+    count = total * a.num_kv_heads;
+    items = sorted;
+  } else {
+    count = *planned_count;
+  }
 
   if (warp < 8) {
     softmax_role<kBf16, G>(a, smem, b, tmem, items, count, warp >> 2, rank);
