@@ -463,14 +463,15 @@ constexpr int kRemBuckets = 256;  // last-split lengths, in 1/256ths of a split
 // Context length of sequence s when it is of the decode class and its
 // lengths are consistent, else 0 (inconsistent ones reported by CTA 0).
 __device__ __forceinline__ int decode_ctx(const AttnArgs& a, int s) {
+  // the three loads go out together (s < num_seqs: every address is in bounds)
   const int q0 = __ldg(a.query_start_loc + s);
   const int qlen = __ldg(a.query_start_loc + s + 1) - q0;
+  const int ctx = __ldg(a.context_lens + s);
   if (q0 < 0 || q0 + qlen > a.num_tokens) {  // query_start_loc inconsistent with num_tokens
     if (blockIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
     return 0;
   }
   if (qlen <= 0 || qlen * a.group > a.decode_max_rows) return 0;  // empty, or handled by the prefill kernel
-  const int ctx = __ldg(a.context_lens + s);
   if (ctx <= 0 || ctx > a.max_blocks_per_seq * a.block_size || ceil_div(ctx, a.split_tokens) > a.max_splits) {
     if (blockIdx.x == 0) report(a.status, KSHIPRA_DEV_BAD_LENGTHS);
     return 0;
