@@ -313,20 +313,18 @@ int kshipra_paged_attention(void* out, const void* q_rot, const void* k_arena, c
  *    query rows from q in registers, and in the CTA whose key split holds a
  *    new token's position the warp that reads that position writes the
  *    token's K and V first;
- *  - otherwise, head_dim 128: the append writes K and V only, then the
- *    attention kernels rotate q themselves (the prefill kernel in shared
- *    memory, the decode kernel in registers) and start while the append
+ *  - otherwise: the append writes K and V only, then the attention kernels
+ *    rotate q themselves (the prefill kernels in shared memory, the decode
+ *    kernel in registers); with head_dim 128 they start while the append
  *    finishes.  This relies on no sequence's new tokens landing in a block
  *    that another sequence of the call reads as its cached prefix (a shared
- *    block is copied before it is written: kshipra_block_make_private);
- *  - otherwise (head_dim 64): the two calls, one after the other.
+ *    block is copied before it is written: kshipra_block_make_private).
  *
  * q [num_tokens][num_q_heads][head_dim], k, v [num_tokens][num_kv_heads]
  * [head_dim], rope_table as for kshipra_kv_append_rope; the other arguments
  * as for kshipra_paged_attention, with the same workspace size.  q_rot
  * (device, [num_tokens][num_q_heads][head_dim]) receives the rotated q; it
- * may be NULL except for head_dim 64 batches with prefill-class rows.  q_rot
- * must not alias out or q.
+ * may be NULL.  q_rot must not alias out or q.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA.
  */
 int kshipra_decode_step(void* out, const void* q, const void* k, const void* v, void* q_rot, void* k_arena,

@@ -269,8 +269,9 @@ def kshipra_paged_attention(out, q_rot, k_arena, v_arena, block_tables, context_
 def kshipra_decode_step(out, q, k, v, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc,
                         positions, rope_table, max_query_len: int, max_context_len: int, scale: float,
                         workspace=None, stream=None) -> None:
-    """RoPE-and-append then attention in one launch for decode-class batches
-    (q_rot may then be None); shapes as in include/kshipra.h."""
+    """RoPE-and-append then attention: one launch for decode-class batches,
+    otherwise a K/V append and attention kernels that rotate q themselves;
+    q_rot may be None.  Shapes as in include/kshipra.h."""
     num_tokens, num_q_heads, head_dim = q.shape
     num_blocks, num_kv_heads, block_size, _ = k_arena.shape
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

@@ -300,8 +300,6 @@ int attention_impl(void* out, const void* q_rot, const void* k_arena, const void
     return fail(KSHIPRA_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, %zu needed", workspace_bytes, plan.total);
   if (plan.total && (!workspace || !aligned(workspace, 256)))
     return fail(KSHIPRA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
-  if (fz && !fz->k && head_dim != 128)
-    return fail(KSHIPRA_ERR_UNSUPPORTED, "in-kernel query rotation needs head_dim 128");
   if (validate_only) return KSHIPRA_OK;
 
   AttnArgs a{};
@@ -515,15 +513,17 @@ int kshipra_decode_step(void* out, const void* q, const void* k, const void* v, 
     if (p && !aligned(p, 16)) return fail(KSHIPRA_ERR_INVALID_ARG, "data pointers must be 16-byte aligned");
   if (q_rot && (q_rot == out || q_rot == q)) return fail(KSHIPRA_ERR_INVALID_ARG, "q_rot must not alias out or q");
   const int group = num_q_heads / num_kv_heads;
-  if (static_cast<long long>(max_query_len) * group > g_opt_decode_max_rows && head_dim == 128) {
-    // rows for the tensor-core prefill kernel: the K/V append, then attention
-    // kernels that rotate q themselves (q_rot optional) and start while the
-    // append finishes; every host check runs before the append is enqueued
+  if (static_cast<long long>(max_query_len) * group > g_opt_decode_max_rows) {
+    // rows for the tensor-core prefill kernels: the K/V append, then attention
+    // kernels that rotate q themselves (q_rot optional); with head_dim 128
+    // they start while the append finishes (launched as its programmatic
+    // dependents).  Every host check runs before the append is enqueued.
+    const bool dependent = head_dim == 128;
     const FusedInputs fz{q, nullptr, nullptr, rope_table, rope_max_pos, q_rot, k_arena, v_arena};
     if ((rc = attention_impl(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc, positions,
                              num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads, num_kv_heads,
                              head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype, workspace,
-                             workspace_bytes, stream, &fz, true, true)))
+                             workspace_bytes, stream, &fz, dependent, true)))
       return rc;
     AppendArgs ap{};
     if ((rc = append_prepare(&ap, nullptr, k, v, nullptr, k_arena, v_arena, block_tables, query_start_loc, positions,
@@ -537,21 +537,7 @@ int kshipra_decode_step(void* out, const void* q, const void* k, const void* v, 
     return attention_impl(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc, positions,
                           num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads, num_kv_heads, head_dim,
                           block_size, max_blocks_per_seq, num_blocks, scale, dtype, workspace, workspace_bytes, stream,
-                          &fz, true, false);
-  }
-  if (static_cast<long long>(max_query_len) * group > g_opt_decode_max_rows) {
-    // head_dim 64 with prefill rows: the two calls, through q_rot
-    if (!q_rot)
-      return fail(KSHIPRA_ERR_INVALID_ARG, "q_rot is required when a sequence has more than %d query rows",
-                  g_opt_decode_max_rows);
-    if ((rc = kshipra_kv_append_rope(q, k, v, q_rot, k_arena, v_arena, block_tables, query_start_loc, positions,
-                                     rope_table, rope_max_pos, num_seqs, num_tokens, num_q_heads, num_kv_heads,
-                                     head_dim, block_size, max_blocks_per_seq, num_blocks, dtype, stream)))
-      return rc;
-    return kshipra_paged_attention(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc,
-                                   positions, num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads,
-                                   num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype,
-                                   workspace, workspace_bytes, stream);
+                          &fz, dependent, false);
   }
   const FusedInputs fz{q, k, v, rope_table, rope_max_pos, q_rot, k_arena, v_arena};
   return attention_impl(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc, positions,

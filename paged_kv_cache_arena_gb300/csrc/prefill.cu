@@ -35,6 +35,9 @@
 //    max is only raised when the row max passes it by 2^8, so O is rarely
 //    rescaled), writes P as fp16/bf16 back into TMEM, and at the end of the
 //    item normalises O and stores the output row.
+// Fused step (q_raw set): Q_A / Q_B are loaded from the raw q; the softmax
+// threads rotate them in place (each its half of its row) and the MMA issuer
+// starts on "Q ready" instead of "Q landed".
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+d), O_B [384,384+d);
 // P_X (two 16-bit values per column) occupies columns [0,32) and [64,96) of
 // S_X, the first half of each softmax thread's own 64 S columns.
@@ -44,6 +47,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "rope.cuh"
 
 namespace kshipra {
 namespace {
@@ -69,8 +73,8 @@ struct PrefillLayout {
   static constexpr int kXBytes = (2 * 2 * 2 + 2 * 2) * kTile * 4;
   static constexpr int kBar = kX + kXBytes;
   // q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-  // p_full[2], o_full[2], o_free[2], drain; then the TMEM base address
-  static constexpr int kNumBars = 19;
+  // p_full[2], o_full[2], o_free[2], drain, q_ready; then the TMEM base address
+  static constexpr int kNumBars = 20;
   static constexpr int kBytes = kBar + kNumBars * 8 + 16;
   static constexpr int kAlloc = kBytes + 1024;
 };
@@ -87,6 +91,7 @@ struct Bars {
   uint64_t* o_full;   // [2]
   uint64_t* o_free;   // [2]
   uint64_t* drain;
+  uint64_t* q_ready;  // fused step: both query tiles rotated (one arrival per softmax thread)
 };
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -370,7 +375,7 @@ __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const
     const PairGeom p = pair_geom<G>(a, it.s, it.pair);
     const int n = p.ntiles;
     if (n == 0) continue;
-    if (!mbar_wait(b.q_full, items_done & 1, a.status)) { ok = false; break; }
+    if (!mbar_wait(a.q_raw != nullptr ? b.q_ready : b.q_full, items_done & 1, a.status)) { ok = false; break; }
     // the previous item's epilogues must have read O_A / O_B before PV overwrites them
     const bool wait_o = items_done > 0;
     const int g0 = g;
@@ -478,6 +483,44 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
     const int tok = row_valid ? p.q0 + p.tok_a + TQ * x + tl : p.q0 + p.tok_a + p.n_a + p.n_b - 1;
     const int pos = __ldg(a.positions + tok);
     float m_ref = kNegInf, l = 0.f;
+    if (a.q_raw != nullptr) {
+      // fused step: this thread's half of row r of the raw Q_x, rotated in
+      // place (the append kernel's float32 arithmetic, bit for bit).  Element
+      // e pairs with e + D/2, so 16-byte chunk c (elements 8c .. 8c+7) pairs
+      // with chunk c + D/16 of the same row; half h takes chunks h D/32 ..
+      // (h + 1) D/32 - 1 and their partners.  The rows go to q_rot when asked,
+      // and every thread reports to the MMA issuer, which starts on "Q ready".
+      if (!warp_wait(b.q_full, items_done & 1, a.status)) { ok = false; break; }
+      if (row_valid) {
+        if (pos < 0 || pos >= a.rope_max_pos) {
+          report(a.status, KSHIPRA_DEV_BAD_POSITION);
+        } else {
+          constexpr int kPairs = D / 16;
+          uint8_t* qrow = smem + (x ? L::kQB : L::kQA) + r * 128;
+          const float* cs = a.rope_table + static_cast<size_t>(pos) * D;
+          uint4* qr = a.q_rot_out == nullptr
+                          ? nullptr
+                          : reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.q_rot_out) +
+                                                     (static_cast<size_t>(tok) * a.num_q_heads + it.h * G + gg) * D);
+#pragma unroll
+          for (int k = 0; k < kPairs / 2; ++k) {
+            const int c = half * (kPairs / 2) + k, cp = c + kPairs;
+            uint4* lo = reinterpret_cast<uint4*>(qrow + (c >> 3) * L::kRegionBytes + (((c & 7) ^ (r & 7)) << 4));
+            uint4* hi = reinterpret_cast<uint4*>(qrow + (cp >> 3) * L::kRegionBytes + (((cp & 7) ^ (r & 7)) << 4));
+            uint4 ylo, yhi;
+            rotate_eight_pairs_vals<kBf16>(*lo, *hi, cs + 16 * c, ylo, yhi);
+            *lo = ylo;
+            *hi = yhi;
+            if (qr != nullptr) {
+              qr[c] = ylo;
+              qr[cp] = yhi;
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();  // the rotated rows visible to the tensor core
+      mbar_arrive(b.q_ready);
+    }
 
     for (int j = 0; j < n; ++j) {
       const int gt = g + j;
@@ -629,7 +672,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  const Bars b{bar, bar + 1, bar + 2, bar + 4, bar + 6, bar + 8, bar + 10, bar + 12, bar + 14, bar + 16, bar + 18};
+  const Bars b{bar,      bar + 1,  bar + 2,  bar + 4,  bar + 6, bar + 8,
+               bar + 10, bar + 12, bar + 14, bar + 16, bar + 18, bar + 19};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + L::kNumBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -647,6 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b.o_free[i], 2 * kTile);
     }
     mbar_init(b.drain, 1);
+    mbar_init(b.q_ready, 4 * kTile);  // every softmax thread of both tiles
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {

@@ -247,8 +247,8 @@ def step_args(mem, **over):
 @pytest.mark.parametrize("over,code", [
     (dict(rope_max_pos=0), 1), (dict(q=None), 1), (dict(table=None), 1), (dict(k=Ptr("k", 8)), 1),
     (dict(dtype=2), 2), (dict(d=96), 2), (dict(hq=6, hkv=4), 1), (dict(q_rot=Ptr("out")), 1),
-    # a 40-token chunk needs the two-call path, which needs q_rot
-    (dict(max_q=40, num_tokens=40, q_rot=None), 1),
+    # a 40-token chunk (prefill kernel path) with q_rot aliasing q
+    (dict(max_q=40, num_tokens=40, q_rot=Ptr("q")), 1),
 ])
 def test_decode_step_validation(lib, mem, over, code):
     assert lib.kshipra_decode_step(*step_args(mem, **over)) == code

@@ -164,11 +164,31 @@ def test_fused_prefill_step_sees_inputs_written_just_before(clean_status):
     assert_close(out_b.float().cpu().numpy().astype(np.float64), oracle.workload_attention(w), w.dtype, "q from b")
 
 
-def test_prefill_rows_head_dim_64_take_the_two_calls(clean_status):
-    # head_dim 64 (one-CTA prefill kernel): append + attention through q_rot
-    w = custom(48, Hq=8, Hkv=2, d=64, prefix=[10, 300], qlen=[40, 1])
+HD64_CASES = {
+    "g4": lambda: custom(48, Hq=8, Hkv=2, d=64, prefix=[10, 300], qlen=[40, 1]),
+    "g1-bf16-bs32": lambda: custom(49, Hq=4, Hkv=4, d=64, bs=32, dtype="bf16", prefix=[0, 500, 77],
+                                   qlen=[130, 200, 3]),
+    "g16-many-tiles": lambda: custom(50, Hq=16, Hkv=1, d=64, prefix=[1200, 0], qlen=[33, 260]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(HD64_CASES))
+def test_fused_prefill_step_head_dim_64(clean_status, name):
+    # head_dim 64 (one-CTA prefill kernel): K/V append, then the prefill
+    # kernel rotating q in shared memory; the arena and q_rot bit for bit, the
+    # output as the two calls give it
+    w = HD64_CASES[name]()
     dw = fused(w)
     ka, va = oracle.workload_arena(w, NAN_SENTINEL)
-    assert np.array_equal(bits_of(dw.k_arena), ka)
+    assert np.array_equal(bits_of(dw.k_arena), ka) and np.array_equal(bits_of(dw.v_arena), va)
     assert np.array_equal(bits_of(dw.q_rot), oracle.workload_q_rot(w))
-    assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype, "two calls")
+    assert_close(dw.out_f64(), oracle.workload_attention(w), w.dtype, "fused step, head_dim 64")
+    assert np.array_equal(bits_of(dw.out), bits_of(two_calls(w).out))
+
+
+def test_fused_prefill_step_head_dim_64_without_q_rot(clean_status):
+    w = custom(51, Hq=8, Hkv=2, d=64, prefix=[10, 300, 0], qlen=[140, 1, 64])
+    dw = fused(w, q_rot=False)
+    ka, va = oracle.workload_arena(w, NAN_SENTINEL)
+    assert np.array_equal(bits_of(dw.k_arena), ka) and np.array_equal(bits_of(dw.v_arena), va)
+    assert np.array_equal(bits_of(dw.out), bits_of(two_calls(w).out))
