@@ -42,6 +42,50 @@ int cuda_fail(cudaError_t e, const char* what) {
 thread_local int g_opt_split_tokens = 0;
 thread_local int g_opt_decode_max_rows = kDecodeMaxRows;
 
+// A mixed batch (decode-class and prefill-class rows, head_dim 128) runs its
+// prefill kernel on a side stream of the calling thread, beside the decode
+// kernel: a fork event on the caller's stream, the pair kernel on the side
+// stream (highest priority, so that its clusters are placed before the
+// decode CTAs fill the SMs), the decode kernel on the caller's stream, and a
+// join event the caller's stream waits for.  Created on first use, one set
+// per (thread, device); released when the thread ends.  Callers that must not
+// create anything (the no-alloc entry point) turn it off for their call.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  int device = -1;
+  ~SideStream() {
+    if (join) cudaEventDestroy(join);
+    if (fork) cudaEventDestroy(fork);
+    if (stream) cudaStreamDestroy(stream);
+  }
+};
+thread_local SideStream g_side[8];
+thread_local bool g_side_off = false;
+
+// The calling thread's side stream on the current device, or null (none
+// could be made, the device index is past the table, or side streams are off).
+SideStream* side_stream() {
+  if (g_side_off) return nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 8) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  SideStream& ss = g_side[dev];
+  if (ss.device == dev) return &ss;
+  int least = 0, greatest = 0;
+  if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;  // the destructor releases whatever was made
+  }
+  ss.device = dev;
+  return &ss;
+}
+
 // ---- device status word ------------------------------------------------
 __device__ unsigned g_status_word;
 
@@ -344,17 +388,31 @@ int attention_impl(void* out, const void* q_rot, const void* k_arena, const void
   const long long qd = a.decode_max_rows / a.group;
   const bool any_decode =
       qd >= 1 && static_cast<long long>(num_tokens) <= static_cast<long long>(num_seqs - 1) * max_query_len + qd;
+  // prefill class: any sequence with more rows than the decode kernel takes
+  const bool any_prefill = static_cast<long long>(max_query_len) * a.group > a.decode_max_rows;
+  CUtensorMap kmap_p, vmap_p;
+  if (any_prefill) {
+    if ((rc = arena_map(&kmap_p, k_arena, dtype, head_dim, rows, block_size))) return rc;
+    if ((rc = arena_map(&vmap_p, v_arena, dtype, head_dim, rows, block_size))) return rc;
+    if ((rc = query_map(&qmap, fz ? fz->q : q_rot, dtype, head_dim, num_q_heads, num_tokens, a.group))) return rc;
+  }
+  SideStream* side = any_decode && any_prefill && head_dim == 128 ? side_stream() : nullptr;
+  if (side) {  // the prefill kernel beside the decode kernel
+    a.beside_decode = 1;
+    if ((e = cudaEventRecord(side->fork, s)) != cudaSuccess) return cuda_fail(e, "side stream fork");
+    if ((e = cudaStreamWaitEvent(side->stream, side->fork, 0)) != cudaSuccess) return cuda_fail(e, "side stream fork");
+    if ((e = launch_prefill(a, kmap_p, vmap_p, qmap, side->stream)) != cudaSuccess)
+      return cuda_fail(e, "prefill kernel launch");
+    if ((e = cudaEventRecord(side->join, side->stream)) != cudaSuccess) return cuda_fail(e, "side stream join");
+  }
   if (any_decode) {
     if (a.ws_counters && (e = cudaMemsetAsync(a.ws_counters, 0, plan.counter_bytes, s)) != cudaSuccess)
       return cuda_fail(e, "clearing split counters");
     if ((e = launch_decode(a, kmap, vmap, s)) != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   }
-  // prefill class: any sequence with more rows than the decode kernel takes
-  if (static_cast<long long>(max_query_len) * a.group > a.decode_max_rows) {
-    CUtensorMap kmap_p, vmap_p;
-    if ((rc = arena_map(&kmap_p, k_arena, dtype, head_dim, rows, block_size))) return rc;
-    if ((rc = arena_map(&vmap_p, v_arena, dtype, head_dim, rows, block_size))) return rc;
-    if ((rc = query_map(&qmap, fz ? fz->q : q_rot, dtype, head_dim, num_q_heads, num_tokens, a.group))) return rc;
+  if (side) {
+    if ((e = cudaStreamWaitEvent(s, side->join, 0)) != cudaSuccess) return cuda_fail(e, "side stream join");
+  } else if (any_prefill) {
     if ((e = launch_prefill(a, kmap_p, vmap_p, qmap, s)) != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
   }
   return KSHIPRA_OK;
@@ -375,6 +433,11 @@ int api_fail(int code, const char* fmt, ...) {
 }
 int api_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 cudaError_t api_status_ptr(unsigned** out) { return status_ptr(out); }
+bool api_side_streams(bool on) {
+  const bool was = !g_side_off;
+  g_side_off = !on;
+  return was;
+}
 }  // namespace kshipra
 
 // ===========================================================================

@@ -601,7 +601,7 @@ cudaError_t launch_decode_f(const AttnArgs& a, const CUtensorMap& kmap, const CU
   const long long units = static_cast<long long>(a.max_splits) * a.num_kv_heads * a.num_seqs;
   if (units > INT_MAX) return cudaErrorInvalidConfiguration;
   return launch_kernel(decode_kernel<D, kBf16, kFused>, dim3(static_cast<unsigned>(units)), dim3(kThreads), L::kAlloc,
-                       stream, true, kmap, vmap, a);
+                       stream, !a.beside_decode, kmap, vmap, a);
 }
 
 template <int D, bool kBf16>

@@ -16,6 +16,9 @@ void api_clear_error();
 int api_fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 int api_cuda_fail(cudaError_t e, const char* what);
 cudaError_t api_status_ptr(unsigned** out);
+// Turns the calling thread's side streams (mixed batches run their prefill
+// kernel beside the decode kernel) off or back on; returns the previous state.
+bool api_side_streams(bool on);
 
 // Rows of (token, q head) a decode unit handles at most: query_len x group.
 constexpr int kDecodeMaxRows = 16;
@@ -83,6 +86,12 @@ struct AttnArgs {
   // its own predecessor has completed) the attention kernels read everything
   // but the arena before that wait
   int early_inputs;
+  // mixed batch, head_dim 128: the pair kernel runs on a side stream beside
+  // the decode kernel and keeps only the clusters its share of the call
+  // needs (the rest leave at once, their SMs going to the decode kernel);
+  // the decode kernel then launches as an ordinary dependent, so that it does
+  // not take the SMs before the pair kernel has placed its clusters
+  int beside_decode;
 };
 
 // Batches of at most this many sequences run their decode units longest

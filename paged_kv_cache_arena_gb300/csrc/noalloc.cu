@@ -63,9 +63,14 @@ extern "C" int kshipra_paged_attention_noalloc(void* out, const void* q_rot, con
   // partials exceed the scratch (KSHIPRA_ERR_WORKSPACE_TOO_SMALL, message in
   // kshipra_last_error) before anything is launched.  Every partial the
   // kernels read is written earlier in the same call, so nothing left by a
-  // previous call needs clearing.
-  return kshipra_paged_attention(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc,
-                                 positions, num_seqs, num_tokens, max_query_len, max_context_len, num_q_heads,
-                                 num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype,
-                                 scratch, KSHIPRA_NOALLOC_SCRATCH_BYTES, stream);
+  // previous call needs clearing.  The call creates nothing either: a mixed
+  // batch runs its kernels one after the other on the caller's stream
+  // instead of on a side stream made on first use.
+  const bool side_was_on = kshipra::api_side_streams(false);
+  const int rc = kshipra_paged_attention(out, q_rot, k_arena, v_arena, block_tables, context_lens, query_start_loc,
+                                         positions, num_seqs, num_tokens, max_query_len, max_context_len,
+                                         num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                         num_blocks, scale, dtype, scratch, KSHIPRA_NOALLOC_SCRATCH_BYTES, stream);
+  kshipra::api_side_streams(side_was_on);
+  return rc;
 }

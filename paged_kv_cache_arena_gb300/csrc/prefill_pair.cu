@@ -90,7 +90,8 @@ struct Layout {
   static constexpr int kPlanSorted = kPlan;                 // [kSortCapacity] sorted entries
   static constexpr int kPlanBuf = kPlanSorted + kSortCapacity * 8;  // [kSortCapacity] listed entries
   static constexpr int kPlanWarp = kPlanBuf + kSortCapacity * 8;   // per-warp totals, running base
-  static constexpr int kBytes = kPlanWarp + 64;
+  static constexpr int kShare = kPlanWarp + 64;                     // [2 x 11] per-warp sums of the share
+  static constexpr int kBytes = kShare + 2 * 11 * 8;
   // the dynamic shared memory of a kernel without static shared variables
   // starts at the base of the CTA's window (1024-aligned, checked at run time)
   static constexpr int kAlloc = kBytes;
@@ -171,8 +172,8 @@ __device__ __forceinline__ Item item_at(const uint64_t* entries, int i, int num_
   return Item{static_cast<int>((v >> 16) & 0xFFFFFF), static_cast<int>(v & 0xFFFF), i % num_kv_heads};
 }
 
-__device__ __forceinline__ int item_index(int r) {
-  const int nc = gridDim.x >> 1, c = blockIdx.x >> 1;
+__device__ __forceinline__ int item_index(int r, int nc) {
+  const int c = blockIdx.x >> 1;
   return r * nc + ((r & 1) ? nc - 1 - c : c);
 }
 
@@ -306,7 +307,8 @@ __device__ __forceinline__ int lane_block_id(const int32_t* table, int j, int nk
 template <int G>
 __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUtensorMap* vmap,
                                               const CUtensorMap* qmap, const AttnArgs& a, uint8_t* smem,
-                                              const Bars& b, const uint64_t* items, int count, uint32_t rank) {
+                                              const Bars& b, const uint64_t* items, int count, int nc,
+                                              uint32_t rank) {
   using L = Layout;
   constexpr int TQ = kTile / G;
   const int lane = threadIdx.x & 31;
@@ -329,7 +331,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
   bool ok = true, waited = !a.early_inputs;
   const bool rotate = a.q_raw != nullptr;
   for (int r = 0; ok; ++r) {
-    const int idx = item_index(r);
+    const int idx = item_index(r, nc);
     if (idx >= count) break;
     const Item it = item_at(items, idx, a.num_kv_heads);
     const QuadGeom p = quad_geom<G>(a, it.s, it.quad, static_cast<int>(rank));
@@ -483,7 +485,7 @@ __device__ __forceinline__ void issue_pv(const Descs& dd, const Bars& b, uint32_
 // both tiles (stage empty, Q empty) count one arrival from each issuer.
 template <bool kBf16, int G>
 __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem,
-                                         const uint64_t* items, int count, int x) {
+                                         const uint64_t* items, int count, int nc, int x) {
   using L = Layout;
   const uint32_t sb = smem_u32(smem);
   Descs dd;
@@ -499,7 +501,7 @@ __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const
   int g = 0, items_done = 0;
 
   for (int r = 0; ok; ++r) {
-    const int idx = item_index(r);
+    const int idx = item_index(r, nc);
     if (idx >= count) break;
     const Item it = item_at(items, idx, a.num_kv_heads);
     const QuadGeom p = quad_geom<G>(a, it.s, it.quad, 0);
@@ -661,7 +663,7 @@ __device__ __forceinline__ void store_rows(const uint8_t* tile, int w, uint16_t*
 // rescaled, and O / l is unchanged.
 template <bool kBf16, int G>
 __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem,
-                                             const uint64_t* items, int count, int x, uint32_t rank) {
+                                             const uint64_t* items, int count, int nc, int x, uint32_t rank) {
   using L = Layout;
   constexpr int TQ = kTile / G;
   constexpr float kRescaleThreshold = 8.f;
@@ -689,7 +691,7 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
   };
   auto find = [&](int ri, RowItem& w) -> int {
     for (;; ++ri) {
-      const int idx = item_index(ri);
+      const int idx = item_index(ri, nc);
       if (idx >= count) return -1;
       w.it = item_at(items, idx, a.num_kv_heads);
       w.p = quad_geom<G>(a, w.it.s, w.it.quad, static_cast<int>(rank));
@@ -848,6 +850,55 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
   }
 }
 
+// ---------------------------------------------------------------- share
+
+// Clusters of this grid that take items when the pair kernel runs beside the
+// decode kernel of the same call.  The decode kernel is bound by HBM
+// bandwidth and needs only part of the SMs to reach it: two CTAs per SM with
+// 96 KB of loads in flight each, against the ~10 MB that HBM needs in flight
+// at full bandwidth, is 56 SMs; it keeps kDecodeClusters clusters' worth and
+// the prefill items take the rest -- unless they would then outlast the
+// decode kernel (the items' key tiles at 4 us per tile and cluster, the rate
+// measured beside the decode kernel's traffic, against the decode-class
+// sequences' K/V bytes at 6.5 TB/s), in which case they take every cluster
+// and the decode kernel fills the SMs they leave.  All threads of the CTA
+// take part; every CTA gets the same answer.
+constexpr int kDecodeClusters = 28;
+
+template <int G>
+__device__ int share_clusters(const AttnArgs& a, const uint64_t* items, int count, int nc, long long* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long keys = 0, tiles = 0;
+  for (int s = threadIdx.x; s < a.num_seqs; s += kThreads) {
+    const int q0 = __ldg(a.query_start_loc + s), ctx = __ldg(a.context_lens + s);
+    const int qlen = __ldg(a.query_start_loc + s + 1) - q0;
+    if (qlen > 0 && qlen * G <= a.decode_max_rows && ctx > 0) keys += ctx;
+  }
+  const int entries = count / a.num_kv_heads;
+  for (int i = threadIdx.x; i < entries; i += kThreads) tiles += static_cast<long long>(items[i] >> 40);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    keys += __shfl_xor_sync(0xffffffffu, keys, off);
+    tiles += __shfl_xor_sync(0xffffffffu, tiles, off);
+  }
+  if (lane == 0) {
+    scratch[warp] = keys;
+    scratch[kThreads / 32 + warp] = tiles;
+  }
+  __syncthreads();
+  keys = tiles = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    keys += scratch[w];
+    tiles += scratch[kThreads / 32 + w];
+  }
+  __syncthreads();  // scratch may be reused
+  const int k = nc - kDecodeClusters;
+  if (k < 1) return nc;
+  const double decode_us = static_cast<double>(keys) * a.num_kv_heads * kD * 4 / 6.5e6;
+  const double prefill_us = 4.0 * static_cast<double>(tiles) * a.num_kv_heads / k;
+  return prefill_us <= decode_us ? k : nc;
+}
+
 // ---------------------------------------------------------------- kernel
 
 template <bool kBf16, int G>
@@ -926,12 +977,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     count = *planned_count;
   }
 
+  // clusters that take items: all of them, or beside the decode kernel only
+  // those its share of the call needs (the others run their roles zero times)
+  int nc = static_cast<int>(gridDim.x >> 1);
+  if (a.beside_decode) nc = share_clusters<G>(a, items, count, nc, reinterpret_cast<long long*>(smem + L::kShare));
+  if (static_cast<int>(blockIdx.x >> 1) >= nc) count = 0;
   if (warp < 8) {
-    softmax_role<kBf16, G>(a, smem, b, tmem, items, count, warp >> 2, rank);
+    softmax_role<kBf16, G>(a, smem, b, tmem, items, count, nc, warp >> 2, rank);
   } else if (warp == kProducerWarp) {
-    producer_role<G>(&kmap, &vmap, &qmap, a, smem, b, items, count, rank);
+    producer_role<G>(&kmap, &vmap, &qmap, a, smem, b, items, count, nc, rank);
   } else if (rank == 0) {
-    if (lane == 0) mma_role<kBf16, G>(a, smem, b, tmem, items, count, warp - kMmaWarp);
+    if (lane == 0) mma_role<kBf16, G>(a, smem, b, tmem, items, count, nc, warp - kMmaWarp);
   }
   grid_dependency_wait();  // (at once when the producer has waited already)
   tc_fence_before();

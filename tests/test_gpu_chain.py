@@ -62,3 +62,44 @@ def test_each_call_sees_the_previous_output(clean_status, name, call):
         assert np.array_equal(a, b)
     # the chain is not trivial: each link changes the values
     assert not np.array_equal(free[0], free[1])
+
+
+def test_mixed_batches_from_two_host_threads(clean_status):
+    # a mixed batch runs its prefill kernel on a side stream of the calling
+    # thread; two threads issuing mixed batches on their own streams at once
+    # must each get the bits they get alone
+    import threading
+    ws = [custom(81, prefix=[100, 600, 2000, 40], qlen=[200, 1, 1, 64]),
+          custom(82, Hq=16, Hkv=4, prefix=[300, 5, 900, 1500], qlen=[1, 150, 1, 1])]
+    dws = [DeviceWorkload(w) for w in ws]
+    refs = []
+    for dw in dws:
+        dw.append_step()
+        dw.attention()
+        torch.cuda.synchronize()
+        refs.append(bits_of(dw.out))
+    results = [None, None]
+    errors = []
+
+    def run(i):
+        try:
+            s = torch.cuda.Stream()
+            outs = []
+            for _ in range(6):
+                o = torch.empty_like(dws[i].out)
+                dws[i].attention(out=o, stream=s)
+                outs.append(o)
+            s.synchronize()
+            results[i] = [bits_of(o) for o in outs]
+        except Exception as exc:  # reported below, on the test's thread
+            errors.append(exc)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(2):
+        for got in results[i]:
+            assert np.array_equal(got, refs[i])
