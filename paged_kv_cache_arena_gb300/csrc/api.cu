@@ -109,10 +109,19 @@ cudaError_t status_ptr(unsigned** out) {
   return cudaSuccess;
 }
 
+// The SM count of the current device.  The first call on a host thread (and
+// after a change of device) also makes the device's primary context current
+// there: the driver-API tensor-map encoder needs one, and a thread whose CUDA
+// work went through other libraries so far may have none bound yet.
 cudaError_t sm_count_current(int* out) {
+  thread_local int bound = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (bound != dev) {
+    if ((e = cudaSetDevice(dev)) != cudaSuccess) return e;
+    bound = dev;
+  }
   return cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
 }
 
