@@ -445,6 +445,9 @@ def measure_workload(torch, stream, pk, name, steps=30):
            "append_ms_per_call": round(app_ms, 5), "step_ms": round(step_ms, 5),
            "step": "kshipra_decode_step (one decode launch with the append inside, or a K/V append then "
                    "attention kernels rotating q themselves)",
+           "attention": "kshipra_paged_attention (decode kernel; with prefill rows too, head_dim 128, the "
+                        "prefill kernel beside it on a side stream)" if flops and len(dec) else
+                        "kshipra_paged_attention",
            "tokens_per_s": round(w.num_tokens / (att_ms * 1e-3), 1),
            "decode_seqs": int(len(dec)), "decode_kv_bytes": kv, "prefill_seqs": int(len(pre)),
            "prefill_flops": flops, "l2": "inputs larger than L2 (%.0f MB of KV read per call)" % (kv / 1e6),
