@@ -103,3 +103,26 @@ def test_mixed_batches_from_two_host_threads(clean_status):
     for i in range(2):
         for got in results[i]:
             assert np.array_equal(got, refs[i])
+
+
+@pytest.mark.parametrize("name", ["mixed-config", "custom"])
+def test_mixed_batch_side_by_side_equals_one_after_the_other(clean_status, name):
+    # kshipra_paged_attention runs a mixed batch's prefill kernel beside the
+    # decode kernel, on a side stream and on part of the SMs; the no-alloc
+    # entry point runs the same kernels one after the other on the caller's
+    # stream: the outputs must be bit-identical
+    from workloads import make_config
+    K = clean_status
+    # (sizes whose split partials fit the no-alloc scratch)
+    w = make_config("mixed") if name == "mixed-config" else custom(
+        83, prefix=[0, 2500] + [(211 * k) % 3000 + 64 for k in range(20)], qlen=[150, 60] + [1, 2] * 10)
+    dw = DeviceWorkload(w)
+    dw.append_step()
+    dw.attention()
+    torch.cuda.synchronize()
+    side = bits_of(dw.out)
+    out = torch.empty_like(dw.out)
+    K.kshipra_paged_attention_noalloc(out, dw.q_rot, dw.k_arena, dw.v_arena, dw.block_tables, dw.context_lens,
+                                      dw.query_start_loc, dw.positions, w.max_query_len, w.max_context_len, w.scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(side, bits_of(out))
