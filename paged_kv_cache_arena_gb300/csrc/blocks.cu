@@ -29,32 +29,57 @@ namespace {
 
 // ---------------------------------------------------------------- block move
 //
-// One CTA per (block i, kv head h): moves the bs x d tile of K and of V from
-// src to dst, 16 bytes per thread per step.  Each side is either the arena
-// (block id from its id list, layout [blocks][Hkv][bs][d]) or a dense buffer
-// [n][Hkv][bs][d] indexed by i (ids == nullptr), which may be pinned host
-// memory reached over the CPU-GPU link.  Ids outside the arena are reported
-// and skipped.
+// One CTA per (block i, group of kMoveHeads kv heads): moves the group's
+// bs x d tiles of K and of V from src to dst.  The group's 16-byte vectors
+// are walked kMoveInFlight per thread at a time, every load of a round issued
+// before its stores, so that each thread keeps several loads in flight (the
+// copy is bound by memory latency x bytes in flight, over HBM and even more
+// over the CPU-GPU link).  Each side is either the arena (block id from its
+// id list, layout [blocks][Hkv][bs][d]) or a dense buffer [n][Hkv][bs][d]
+// indexed by i (ids == nullptr), which may be pinned host memory reached over
+// the CPU-GPU link.  Ids outside the arena are reported and skipped.
+// Launched as a programmatic dependent of the previous grid, it waits for it
+// before touching memory.
 constexpr int kMoveThreads = 256;
+constexpr int kMoveHeads = 4;
+constexpr int kMoveInFlight = 2;  // vectors of K (and of V) per thread per round
 
 __global__ void __launch_bounds__(kMoveThreads) block_move_kernel(uint4* dst_k, uint4* dst_v, const int32_t* dst_ids,
                                                                   const uint4* src_k, const uint4* src_v,
                                                                   const int32_t* src_ids, int num_kv_heads,
                                                                   int tile_vec, int num_blocks, unsigned* status) {
-  const int i = blockIdx.x, h = blockIdx.y;
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int i = blockIdx.x, h0 = blockIdx.y * kMoveHeads;
   const int sb = src_ids ? __ldg(src_ids + i) : i;
   const int db = dst_ids ? __ldg(dst_ids + i) : i;
   if ((src_ids && (sb < 0 || sb >= num_blocks)) || (dst_ids && (db < 0 || db >= num_blocks))) {
-    if (h == 0 && threadIdx.x == 0) report(status, KSHIPRA_DEV_BAD_BLOCK_ID);
+    if (blockIdx.y == 0 && threadIdx.x == 0) report(status, KSHIPRA_DEV_BAD_BLOCK_ID);
     return;
   }
-  const size_t s0 = (static_cast<size_t>(sb) * num_kv_heads + h) * tile_vec;
-  const size_t d0 = (static_cast<size_t>(db) * num_kv_heads + h) * tile_vec;
-  for (int j = threadIdx.x; j < tile_vec; j += kMoveThreads) {
-    const uint4 kv = src_k[s0 + j];
-    const uint4 vv = src_v[s0 + j];
-    dst_k[d0 + j] = kv;
-    dst_v[d0 + j] = vv;
+  // the group's tiles are contiguous on both sides: heads h0 .. h0 + nh - 1
+  const int nh = min(kMoveHeads, num_kv_heads - h0);
+  const int total = nh * tile_vec;
+  const size_t s0 = (static_cast<size_t>(sb) * num_kv_heads + h0) * tile_vec;
+  const size_t d0 = (static_cast<size_t>(db) * num_kv_heads + h0) * tile_vec;
+  for (int base = threadIdx.x; base < total; base += kMoveThreads * kMoveInFlight) {
+    uint4 kv[kMoveInFlight], vv[kMoveInFlight];
+#pragma unroll
+    for (int u = 0; u < kMoveInFlight; ++u) {
+      const int j = base + u * kMoveThreads;
+      if (j < total) {
+        kv[u] = src_k[s0 + j];
+        vv[u] = src_v[s0 + j];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kMoveInFlight; ++u) {
+      const int j = base + u * kMoveThreads;
+      if (j < total) {
+        dst_k[d0 + j] = kv[u];
+        dst_v[d0 + j] = vv[u];
+      }
+    }
   }
 }
 
@@ -98,12 +123,12 @@ int move_blocks(void* dst_k, void* dst_v, const int32_t* dst_ids, const void* sr
   cudaError_t e = api_status_ptr(&status);
   if (e != cudaSuccess) return api_cuda_fail(e, "status word");
   const int tile_vec = block_size * head_dim * 2 / 16;
-  dim3 grid(n, num_kv_heads);
-  block_move_kernel<<<grid, kMoveThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<uint4*>(const_cast<void*>(dev[0])), static_cast<uint4*>(const_cast<void*>(dev[1])), dst_ids,
-      static_cast<const uint4*>(dev[2]), static_cast<const uint4*>(dev[3]), src_ids, num_kv_heads, tile_vec,
-      num_blocks, status);
-  if ((e = cudaGetLastError()) != cudaSuccess) return api_cuda_fail(e, "block move kernel launch");
+  dim3 grid(n, (num_kv_heads + kMoveHeads - 1) / kMoveHeads);
+  e = launch_kernel(block_move_kernel, grid, dim3(kMoveThreads), 0, static_cast<cudaStream_t>(stream), true,
+                    static_cast<uint4*>(const_cast<void*>(dev[0])), static_cast<uint4*>(const_cast<void*>(dev[1])),
+                    dst_ids, static_cast<const uint4*>(dev[2]), static_cast<const uint4*>(dev[3]), src_ids,
+                    num_kv_heads, tile_vec, num_blocks, status);
+  if (e != cudaSuccess) return api_cuda_fail(e, "block move kernel launch");
   return KSHIPRA_OK;
 }
 
