@@ -285,8 +285,8 @@ int kshipra_paged_attention_workspace_size(int num_seqs, int num_tokens, int max
  * splits in `workspace`, merged inside the same kernel by the split that
  * finishes last); the others on a tcgen05 tensor-core chunked-prefill kernel with
  * fully masked key tiles skipped.  The split is decided on the device, so
- * one call may mix both kinds.  When both kinds may be present (head_dim 128),
- * the prefill kernel runs beside the decode kernel: on a side stream of the
+ * one call may mix both kinds.  When both kinds may be present, the prefill
+ * kernel runs beside the decode kernel: on a side stream of the
  * calling thread (created on first use, highest priority, released when the
  * thread ends), forked from and joined back into `stream` with events, so the
  * call stays ordered on `stream` as a whole and can be captured in a CUDA

@@ -405,7 +405,7 @@ int attention_impl(void* out, const void* q_rot, const void* k_arena, const void
     if ((rc = arena_map(&vmap_p, v_arena, dtype, head_dim, rows, block_size))) return rc;
     if ((rc = query_map(&qmap, fz ? fz->q : q_rot, dtype, head_dim, num_q_heads, num_tokens, a.group))) return rc;
   }
-  SideStream* side = any_decode && any_prefill && head_dim == 128 ? side_stream() : nullptr;
+  SideStream* side = any_decode && any_prefill ? side_stream() : nullptr;
   if (side) {  // the prefill kernel beside the decode kernel
     a.beside_decode = 1;
     if ((e = cudaEventRecord(side->fork, s)) != cudaSuccess) return cuda_fail(e, "side stream fork");

@@ -130,8 +130,8 @@ __device__ __forceinline__ Item item_at(const uint64_t* entries, int i, int num_
 }
 
 // Index of this CTA's r-th item (snake order over the sorted list).
-__device__ __forceinline__ int item_index(int r) {
-  return r * gridDim.x + ((r & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
+__device__ __forceinline__ int item_index(int r, int nc) {
+  return r * nc + ((r & 1) ? nc - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
 }
 
 struct PairGeom {
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const AttnAr
 template <int D, int G>
 __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUtensorMap* vmap,
                                               const CUtensorMap* qmap, const AttnArgs& a, uint8_t* smem,
-                                              const Bars& b, const uint64_t* items, int count) {
+                                              const Bars& b, const uint64_t* items, int count, int nc) {
   using L = PrefillLayout<D>;
   constexpr int TQ = kTile / G;
   prefetch_tensormap(qmap);
@@ -244,7 +244,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* kmap, const CUt
   int issued_k0 = 0, issued_k1 = 0, issued_v0 = 0, issued_v1 = 0;  // last tile + 1 per stage
   bool ok = true;
   for (int r = 0; ok; ++r) {
-    const int idx = item_index(r);
+    const int idx = item_index(r, nc);
     if (idx >= count) break;
     const Item it = item_at(items, idx, a.num_kv_heads);
     const PairGeom p = pair_geom<G>(a, it.s, it.pair);
@@ -353,7 +353,7 @@ __device__ __forceinline__ void issue_pv(const Descs& dd, uint32_t tmem, int x, 
 
 template <int D, bool kBf16, int G>
 __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem,
-                                         const uint64_t* items, int count) {
+                                         const uint64_t* items, int count, int nc) {
   using L = PrefillLayout<D>;
   const uint32_t sb = smem_u32(smem);
   Descs dd;
@@ -369,7 +369,7 @@ __device__ __forceinline__ void mma_role(const AttnArgs& a, uint8_t* smem, const
   int g = 0, items_done = 0;
 
   for (int r = 0; ok; ++r) {
-    const int idx = item_index(r);
+    const int idx = item_index(r, nc);
     if (idx >= count) break;
     const Item it = item_at(items, idx, a.num_kv_heads);
     const PairGeom p = pair_geom<G>(a, it.s, it.pair);
@@ -447,7 +447,7 @@ __device__ __forceinline__ void pair_sync(int id) {
 // their partial row maxima every key tile and their partial sums at the end.
 template <int D, bool kBf16, int G>
 __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, const Bars& b, uint32_t tmem,
-                                             const uint64_t* items, int count, int x, int half) {
+                                             const uint64_t* items, int count, int nc, int x, int half) {
   using L = PrefillLayout<D>;
   constexpr int TQ = kTile / G;
   constexpr int HC = kTile / 2;  // key columns per thread
@@ -470,7 +470,7 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
   bool ok = true;
 
   for (int ri = 0; ok; ++ri) {
-    const int idx = item_index(ri);
+    const int idx = item_index(ri, nc);
     if (idx >= count) break;
     const Item it = item_at(items, idx, a.num_kv_heads);
     const PairGeom p = pair_geom<G>(a, it.s, it.pair);
@@ -659,6 +659,53 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, uint8_t* smem, c
   }
 }
 
+// ---------------------------------------------------------------- share
+
+// CTAs of this grid that take items when the kernel runs beside the decode
+// kernel of the same call (the same rule as the head_dim 128 kernel's): the
+// decode kernel, bound by HBM bandwidth, keeps the 56 SMs whose CTAs hold
+// the ~10 MB of loads in flight that full bandwidth needs (its head_dim 64
+// CTAs are half as large, so four fit per SM), and the prefill items take
+// the rest -- unless they would then outlast the decode kernel (key tiles of
+// a tile pair at 4 us per tile and SM beside the decode traffic, against the
+// decode-class sequences' K/V bytes at 6.5 TB/s), when they take every SM.
+// All threads of the CTA take part; every CTA gets the same answer.
+constexpr int kDecodeSms = 56;
+
+template <int D, int G>
+__device__ int share_ctas(const AttnArgs& a, const uint64_t* items, int count, int nc) {
+  __shared__ long long part[2][kThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long keys = 0, tiles = 0;
+  for (int s = threadIdx.x; s < a.num_seqs; s += kThreads) {
+    const int q0 = __ldg(a.query_start_loc + s), ctx = __ldg(a.context_lens + s);
+    const int qlen = __ldg(a.query_start_loc + s + 1) - q0;
+    if (qlen > 0 && qlen * G <= a.decode_max_rows && ctx > 0) keys += ctx;
+  }
+  const int entries = count / a.num_kv_heads;
+  for (int i = threadIdx.x; i < entries; i += kThreads) tiles += static_cast<long long>(items[i] >> 40);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    keys += __shfl_xor_sync(0xffffffffu, keys, off);
+    tiles += __shfl_xor_sync(0xffffffffu, tiles, off);
+  }
+  if (lane == 0) {
+    part[0][warp] = keys;
+    part[1][warp] = tiles;
+  }
+  __syncthreads();
+  keys = tiles = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    keys += part[0][w];
+    tiles += part[1][w];
+  }
+  const int k = nc - kDecodeSms;
+  if (k < 1) return nc;
+  const double decode_us = static_cast<double>(keys) * a.num_kv_heads * D * 4 / 6.5e6;
+  const double prefill_us = 4.0 * static_cast<double>(tiles) * a.num_kv_heads / k;
+  return prefill_us <= decode_us ? k : nc;
+}
+
 // ---------------------------------------------------------------- kernel
 
 template <int D, bool kBf16, int G>
@@ -668,7 +715,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const int* count_ptr) {
   using L = PrefillLayout<D>;
   const int count = *count_ptr;
-  if (static_cast<int>(blockIdx.x) >= count) return;  // no item for this CTA
+  // CTAs that take items: all of them, or beside the decode kernel only
+  // those the prefill items' share of the call needs
+  const int nc = a.beside_decode ? share_ctas<D, G>(a, items, count, static_cast<int>(gridDim.x))
+                                 : static_cast<int>(gridDim.x);
+  if (static_cast<int>(blockIdx.x) >= min(count, nc)) return;  // no item for this CTA
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
@@ -704,11 +755,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 16) {
-    softmax_role<D, kBf16, G>(a, smem, b, tmem, items, count, warp >> 3, (warp >> 2) & 1);
+    softmax_role<D, kBf16, G>(a, smem, b, tmem, items, count, nc, warp >> 3, (warp >> 2) & 1);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<D, G>(&kmap, &vmap, &qmap, a, smem, b, items, count);
+    if (lane == 0) producer_role<D, G>(&kmap, &vmap, &qmap, a, smem, b, items, count, nc);
   } else {
-    if (lane == 0) mma_role<D, kBf16, G>(a, smem, b, tmem, items, count);
+    if (lane == 0) mma_role<D, kBf16, G>(a, smem, b, tmem, items, count, nc);
   }
   tc_fence_before();
   __syncthreads();

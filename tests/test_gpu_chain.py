@@ -105,7 +105,7 @@ def test_mixed_batches_from_two_host_threads(clean_status):
             assert np.array_equal(got, refs[i])
 
 
-@pytest.mark.parametrize("name", ["mixed-config", "custom"])
+@pytest.mark.parametrize("name", ["mixed-config", "custom", "custom-d64"])
 def test_mixed_batch_side_by_side_equals_one_after_the_other(clean_status, name):
     # kshipra_paged_attention runs a mixed batch's prefill kernel beside the
     # decode kernel, on a side stream and on part of the SMs; the no-alloc
@@ -114,8 +114,11 @@ def test_mixed_batch_side_by_side_equals_one_after_the_other(clean_status, name)
     from workloads import make_config
     K = clean_status
     # (sizes whose split partials fit the no-alloc scratch)
-    w = make_config("mixed") if name == "mixed-config" else custom(
-        83, prefix=[0, 2500] + [(211 * k) % 3000 + 64 for k in range(20)], qlen=[150, 60] + [1, 2] * 10)
+    if name == "mixed-config":
+        w = make_config("mixed")
+    else:
+        w = custom(83, d=64 if name == "custom-d64" else 128,
+                   prefix=[0, 2500] + [(211 * k) % 3000 + 64 for k in range(20)], qlen=[150, 60] + [1, 2] * 10)
     dw = DeviceWorkload(w)
     dw.append_step()
     dw.attention()
